@@ -1,0 +1,391 @@
+"""Benchmark: blockwise attention forward + log-sum-exp merge on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the whole path over one batch of the workload: for a
+ring-chunked workload, P attn_partial launches (one per KV chunk, zero-copy
+views) and one lse_merge; for a single-pass workload, one attn_fwd. The
+default workload is the ring-chunked causal attention B=2, H=32, S=4096,
+D=128 with P=8 chunks of 512.
+
+metric: causal-adjusted attention TFLOP/s, F = 4*B*Hq*S^2*D (halved when
+causal), over the step time; the JSON line also carries the dominant
+kernel's roofline, the merge's GB/s, an end-to-end figure through the C ABI
+with host buffers, and the fp64 oracle timed on the host cores.
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload (there is no other implementation of this path to run).
+
+Under torchrun (N > 1) every rank runs an independent replica (the path
+needs no exchange when chunks are emulated on one GPU); value = total FLOPs
+of all ranks / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s (causal-adjusted) & % BF16 peak; lse_merge GB/s & % HBM"
+DEFAULT_WORKLOAD = "ring8_b2h32s4096d128_causal"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129e6
+
+
+# ----------------------------------------------------------------- helpers (host logic, unit-tested on CPU)
+
+def load_peaks(path: str = os.path.join(ROOT, "MEASURED_PEAKS.json")):
+    """(peaks, source) from the measured file when present, else the fallback figures."""
+    try:
+        with open(path) as f:
+            raw = json.load(f)
+        peaks = {}
+        for key in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+            val = raw.get(key)
+            if isinstance(val, dict):
+                val = val.get("value")
+            if isinstance(val, (int, float)) and val > 0:
+                peaks[key] = float(val)
+        if "hbm_gbs" in peaks and "bf16_tflops" in peaks:
+            peaks.setdefault("bf16_tflops_sustained", peaks["bf16_tflops"])
+            return peaks, "measured"
+    except (OSError, ValueError):
+        pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def visible_pairs(S_q: int, q_off: int, kv_len: int, kv_off: int, causal: bool) -> int:
+    """Number of (query, key) pairs a chunk's attention visits exactly."""
+    if not causal:
+        return S_q * kv_len
+    total = 0
+    # row r sees keys j < kv_len with kv_off + j <= q_off + r
+    r = np.arange(S_q, dtype=np.int64)
+    n = np.clip(q_off + r - kv_off + 1, 0, kv_len)
+    total = int(n.sum())
+    return total
+
+
+def merge_algorithmic_bytes(w: workloads.Workload, out_bytes: int = 2) -> int:
+    """Bytes the merge must move: every lse_i, the O_i rows with finite lse_i,
+    the merged O and lse."""
+    rows = w.B * w.Hq * w.S
+    finite_rows = 0
+    C = w.chunk
+    for c in range(w.P):
+        finite_rows += w.B * w.Hq * (w.S - c * C if w.causal else w.S)
+    return w.P * rows * 4 + finite_rows * w.D * 4 + rows * w.D * out_bytes + rows * 4
+
+
+def max_over_ranks(value: float) -> float:
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        t = torch.tensor([value], dtype=torch.float64,
+                         device="cuda" if dist.get_backend() == "nccl" else "cpu")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+    return value
+
+
+def summarise_clocks(lines):
+    """Median SM clock, max clock and the throttle reasons seen in nvidia-smi CSV lines."""
+    sm, mx, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            sm.append(float(parts[1]))
+            mx.append(float(parts[2]))
+        except ValueError:
+            continue
+        for name, flag in zip(names, parts[5:9]):
+            if flag.lower() == "active":
+                reasons.add(name)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+            "samples": len(sm)}
+
+
+class ClockSampler:
+    """nvidia-smi polled every 200 ms while the GPU works; read-only."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                                          "-i", str(index), "-lms", "200"], stdout=self.file,
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        lines = self.file.read().splitlines()
+        self.file.close()
+        os.unlink(self.file.name)
+        return summarise_clocks(lines)
+
+
+# ----------------------------------------------------------------- the GPU arm
+
+def run_ours(args, w: workloads.Workload, rank: int, world: int):
+    import sequence_attn_fwd_gb300 as sa
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    q_h, k_h, v_h = workloads.make_qkv(w)
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    B, Hq, S, D, P, C = w.B, w.Hq, w.S, w.D, w.P, w.chunk
+    o = torch.empty((B, Hq, S, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=dev)
+    o_parts = lse_parts = None
+    if P > 1:
+        o_parts = torch.empty((P, B, Hq, S, D), dtype=torch.float32, device=dev)
+        lse_parts = torch.empty((P, B, Hq, S), dtype=torch.float32, device=dev)
+    launches_per_step = P + 1 if P > 1 else 1
+
+    def step(qq, kk, vv, ev=None):
+        if P == 1:
+            if ev:
+                ev[0].record(stream)
+            sa.attn_fwd(qq, kk, vv, causal=w.causal, out=o, lse=lse)
+            if ev:
+                ev[1].record(stream)
+            return
+        if ev:
+            ev[0].record(stream)
+        for j in range(P):
+            sa.attn_partial(qq, kk[:, :, j * C:(j + 1) * C], vv[:, :, j * C:(j + 1) * C], 0, j * C, w.causal,
+                            out=o_parts[j], lse=lse_parts[j])
+        if ev:
+            ev[1].record(stream)
+        sa.lse_merge(o_parts, lse_parts, torch.bfloat16, out=o, lse=lse)
+        if ev:
+            ev[2].record(stream)
+
+    F = w.attention_flops()
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    # warm-up: at least W steps and about a second of work so clocks settle
+    t_end = time.time() + 1.0
+    n = 0
+    while n < args.warmup or time.time() < t_end:
+        step(q, k, v)
+        n += 1
+        if n % 8 == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(q, k, v, evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    sa.query_device_error(dev)
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1))
+    ms_per_step = elapsed_ms / args.steps
+    attn_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    merge_ms = [e[1].elapsed_time(e[2]) for e in evs] if P > 1 else []
+    value = world * F * args.steps / (elapsed_ms * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host inputs in, host result out
+    e2e = None
+    if rank == 0:
+        q_p, k_p, v_p = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
+        o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        lse_host = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def e2e_step():
+            qd.copy_(q_p, non_blocking=True)
+            kd.copy_(k_p, non_blocking=True)
+            vd.copy_(v_p, non_blocking=True)
+            step(qd, kd, vd)
+            o_host.copy_(o, non_blocking=True)
+            lse_host.copy_(lse, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        n_e2e = max(3, min(args.steps, 20))
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b_.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = a.elapsed_time(b_) / n_e2e
+        h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h))
+        d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+        e2e = {"value": F / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        del qd, kd, vd
+
+    peaks, peak_src = load_peaks()
+    attn_avg_ms = statistics.mean(attn_ms) / (P if P > 1 else 1)  # per launch
+    flops_per_launch = F / (P if P > 1 else 1)
+    achieved = flops_per_launch / (attn_avg_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                "kernel": "attn_fwd_kernel<128,f32 out> (attn_partial)" if P > 1 else "attn_fwd_kernel<128,bf16 out>",
+                "peak_source": f"{peak_src} bf16 burst", "launch_ms": attn_avg_ms}
+    merge = None
+    if merge_ms:
+        mb = merge_algorithmic_bytes(w)
+        mms = statistics.mean(merge_ms)
+        gbs = mb / (mms * 1e-3) / 1e9
+        merge = {"achieved": gbs, "unit": "GB/s", "peak": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"],
+                 "launch_ms": mms, "algorithmic_bytes": mb, "peak_source": f"{peak_src} copy"}
+    return {
+        "value": value, "ms_per_step": ms_per_step, "e2e": e2e, "roofline": roofline, "merge": merge,
+        "gpu_launches": args.steps * launches_per_step, "clocks": clocks,
+        "attn_ms_per_step": statistics.mean(attn_ms),
+    }
+
+
+# ----------------------------------------------------------------- the CPU oracle arm
+
+def oracle_sample(w: workloads.Workload, budget_s: float, q=None, k=None, v=None):
+    """Times the fp64 oracle on whole (batch, head) problems of the workload,
+    one head at a time, until about budget_s seconds of CPU work are done.
+    Returns (TFLOP/s, seconds, heads done, threads)."""
+    import oracle
+
+    if q is None:
+        q, k, v = workloads.make_qkv(w)
+    threads = oracle.default_threads()
+    per_head = w.attention_flops() / (w.B * w.Hq)
+    done = 0
+    t0 = time.perf_counter()
+    g = w.Hq // w.Hkv
+    for bh in range(w.B * w.Hq):
+        b, h = divmod(bh, w.Hq)
+        oracle.attention(q[b:b + 1, h:h + 1], k[b:b + 1, h // g:h // g + 1], v[b:b + 1, h // g:h // g + 1],
+                         w.causal, threads=threads)
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    secs = time.perf_counter() - t0
+    return done * per_head / secs / 1e12, secs, done, threads
+
+
+def run_reference(args, w):
+    q, k, v = workloads.make_qkv(w)
+    for _ in range(args.warmup):
+        oracle_sample(w, 0.0, q, k, v)  # one head
+    rates, secs_all, heads = [], 0.0, 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        r, s, n, threads = oracle_sample(w, args.reference_budget, q, k, v)
+        rates.append(r)
+        secs_all += s
+        heads += n
+    elapsed = time.perf_counter() - t0
+    value = sum(rates) / len(rates)
+    sample = (f"{heads} whole (batch, head) attention problems of the workload over {args.steps} steps "
+              f"(about {args.reference_budget:.0f} s of CPU work per step); fp64 definition, all rows")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def workload_config(w: workloads.Workload):
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "D": w.D, "causal": w.causal,
+            "P": w.P, "chunk": w.chunk, "scale": "1/sqrt(D)",
+            "l2": "no flush: each step writes P fp32 partials and reads them back "
+                  "(>1 GB for ring workloads, inputs >129 MB L2 for single-pass ones)"}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--reference-budget", type=float, default=3.0, help="CPU seconds per reference step")
+    ap.add_argument("--cpu-baseline-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)
+    w = workloads.WORKLOADS[args.workload]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        if args.impl == "reference":
+            if rank != 0:
+                return 0
+        else:
+            dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if args.impl == "reference":
+        print(json.dumps(run_reference(args, w)), flush=True)
+        return 0
+
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}))
+        return 1
+    r = run_ours(args, w, rank, world)
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            val, secs, heads, threads = oracle_sample(w, args.cpu_baseline_budget)
+            cpu = {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                   "sample": f"{heads} whole (batch, head) attention problems of the workload "
+                             f"({secs:.1f} s), fp64, all rows"}
+        line = {"metric": METRIC, "value": r["value"], "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": workload_config(w), "roofline": r["roofline"], "merge": r["merge"],
+                "cpu_baseline": cpu, "e2e": r["e2e"], "gpu_launches": r["gpu_launches"], "clocks": r["clocks"]}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,122 @@
+/*
+ * seqattn -- blockwise exact attention and log-sum-exp merge for GB300 (sm_103a).
+ *
+ * C ABI of libseqattn.so. Every entry point takes plain device pointers and
+ * sizes, enqueues its kernels on the caller's CUDA stream and returns a status
+ * code; nothing is thrown across this boundary and no call synchronises,
+ * except attn_query_device_error().
+ *
+ * Common conventions
+ *   Layout     Q and O are [B, Hq, S, D], K and V are [B, Hkv, S, D], lse is
+ *              [B, Hq, S]; all row-major with D innermost (the [B, H, L, D]
+ *              layout of the listings on page "Ulysses与Ring-Attention序列并行
+ *              技术详解").
+ *   GQA        query head hq reads KV head hq / (Hq / Hkv); Hq % Hkv == 0.
+ *   scale      multiplies Q K^T before the softmax; pass 1/sqrt(D) for the
+ *              pages' scaling. Must be finite and > 0.
+ *   lse        natural logarithm of the softmax normaliser of each query row:
+ *              lse = ln(sum_j exp(scale * q . k_j)) over the visible keys.
+ *   Masking    with causal != 0, query row r (global position q_off + r) sees
+ *              key j (global position kv_off + j) iff kv_off + j <= q_off + r.
+ *              A row that sees no key gets O = 0 and lse = -inf.
+ *   Ownership  all buffers are allocated and owned by the caller; the library
+ *              allocates no device memory. Pointers must be 16-byte aligned.
+ *   Inputs     must be finite (inf/NaN inputs give unspecified outputs).
+ *   Empty      B == 0, S == 0 (or Sq == 0) is a valid no-op returning ATTN_OK.
+ *   Errors     invalid arguments return ATTN_ERR_INVALID_ARG or
+ *              ATTN_ERR_UNSUPPORTED before anything is launched; a failed launch
+ *              returns ATTN_ERR_CUDA (the cudaError_t is kept for
+ *              attn_last_cuda_error()). Device-side waits are bounded: a wait
+ *              that runs out records a code that attn_query_device_error()
+ *              reports as ATTN_ERR_TIMEOUT.
+ */
+#ifndef SEQATTN_H
+#define SEQATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *attn_stream_t;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size or stride */
+    ATTN_ERR_UNSUPPORTED = 2, /* head dim other than 64 or 128, shape past limits */
+    ATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+    ATTN_ERR_TIMEOUT = 4      /* a device-side wait ran out (see attn_query_device_error) */
+} attn_status;
+
+typedef enum { ATTN_BF16 = 0, ATTN_F32 = 1 } attn_dtype;
+
+/*
+ * attn_fwd -- exact attention softmax(scale * Q K^T) V in one pass, computed
+ * tile by tile over K/V with a running maximum and normaliser (the tiled
+ * online-softmax forward of page "ms-swift集成FlashAttention 2/3，长文本训练
+ * 更高效", section "FlashAttention 如何破局？不只是融合内核"); the scores never
+ * reach memory.
+ *
+ *   q    bf16 [B, Hq, S, D]            k, v  bf16 [B, Hkv, S, D]
+ *   o    bf16 [B, Hq, S, D] (output)   lse   fp32 [B, Hq, S] (output)
+ *   D    64 or 128.  causal: 0 or 1 (q_off = kv_off = 0).
+ */
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+             int Hkv, int S, int D, int causal, float scale, attn_stream_t stream);
+
+/*
+ * attn_partial -- attention of a block of queries against one chunk of keys
+ * and values: the per-hop partial result of Ring-Attention (page
+ * "Ulysses与Ring-Attention序列并行技术详解", Ring-Attention part: each hop
+ * attends the local queries to the K/V chunk just received). The result is
+ * normalised within the chunk and carries its own lse, ready for lse_merge.
+ *
+ *   q         bf16 [B, Hq, Sq, D], contiguous.
+ *   k_chunk, v_chunk  bf16; key t of KV head (b, h) is the D contiguous values at
+ *             k_chunk + ((b*Hkv + h) * kv_head_stride + t*D). kv_head_stride is
+ *             in elements; 0 means Skv*D (a contiguous [B,Hkv,Skv,D] chunk). A
+ *             chunk of a larger [B,Hkv,S,D] tensor is passed without a copy as
+ *             k + j0*D with kv_head_stride = S*D. Must be a multiple of 8.
+ *   q_off, kv_off  global positions of query row 0 and key 0 (used by causal).
+ *   o_part    fp32 [B, Hq, Sq, D] (output, normalised by the chunk's softmax
+ *             sum; rows that see no key of the chunk are 0).
+ *   lse_part  fp32 [B, Hq, Sq] (output; -inf where the row sees no key).
+ */
+int attn_partial(const void *q, const void *k_chunk, const void *v_chunk, long long q_off,
+                 long long kv_off, long long kv_head_stride, float *o_part, float *lse_part,
+                 int B, int Hq, int Hkv, int Sq, int Skv, int D, int causal, float scale,
+                 attn_stream_t stream);
+
+/*
+ * lse_merge -- combine P partial results per query row in log space (the
+ * output_acc / logsumexp_acc accumulation of page "Ulysses与Ring-Attention序列
+ * 并行技术详解", Ring-Attention part, read per row with an empty accumulator
+ * at lse = -inf):
+ *     M = max_i lse_i,  w_i = exp(lse_i - M),  lse = M + ln(sum_i w_i),
+ *     O = sum_i w_i O_i / sum_i w_i;   all lse_i = -inf  ->  O = 0, lse = -inf.
+ * Partials with lse_i = -inf are not read.
+ *
+ *   o_parts   fp32 [P, B, H, S, D]     lse_parts  fp32 [P, B, H, S]
+ *   o         [B, H, S, D], bf16 or fp32 per o_dtype (output). With ATTN_F32 it
+ *             may be o_parts itself (part 0), merged in place.
+ *   lse       fp32 [B, H, S] (output; may be lse_parts itself).
+ *   P >= 1, D 64 or 128.
+ */
+int lse_merge(const float *o_parts, const float *lse_parts, int P, void *o, int o_dtype,
+              float *lse, int B, int H, int S, int D, attn_stream_t stream);
+
+/* Synchronises `stream`, then returns ATTN_OK, or ATTN_ERR_TIMEOUT if a kernel
+ * recorded a timed-out wait since the last query (the record is cleared), or
+ * ATTN_ERR_CUDA if the synchronisation failed. */
+int attn_query_device_error(attn_stream_t stream);
+
+/* Static English text for a status code. */
+const char *attn_status_string(int status);
+
+/* The cudaError_t of the most recent ATTN_ERR_CUDA (0 if none). */
+int attn_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SEQATTN_H */

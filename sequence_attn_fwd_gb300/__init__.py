@@ -1,0 +1,154 @@
+"""Blockwise exact attention and log-sum-exp merge on GB300 (sm_103a).
+
+Thin Python binding over the C ABI of ``libseqattn.so`` (include/seqattn.h):
+it checks dtypes, shapes and layouts, marshals pointers and the current CUDA
+stream, and raises on a non-zero status. Every step of the computation runs
+in the library's CUDA kernels; there is no other implementation to fall back
+to, and a missing library is an error.
+
+    o, lse = attn_fwd(q, k, v, causal=True)
+    o_i, lse_i = attn_partial(q, k[:, :, a:b], v[:, :, a:b], q_off=0, kv_off=a, causal=True)
+    o, lse = lse_merge(o_parts, lse_parts)
+    o, lse = ring_attn_fwd(q, k, v, P=8, causal=True)   # P chunks + merge on one GPU
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from ._lib import AttnError, lib
+
+__all__ = ["attn_fwd", "attn_partial", "lse_merge", "ring_attn_fwd", "query_device_error",
+           "AttnError", "lib"]
+
+ATTN_BF16, ATTN_F32 = 0, 1
+
+
+def _stream_handle(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise AttnError(status, what)
+
+
+def _require(cond: bool, msg: str) -> None:
+    if not cond:
+        raise ValueError(msg)
+
+
+def _rows_contiguous(t: torch.Tensor) -> bool:
+    """[B, H, S, D] with D and S packed (row r of a head at r*D) and heads at a
+    uniform stride, so a slice along S of a contiguous tensor qualifies."""
+    B, H, S, D = t.shape
+    return (t.stride(3) == 1 and (S <= 1 or t.stride(2) == D)
+            and (B <= 1 or t.stride(0) == H * t.stride(1)))
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+             scale: float | None = None, out: torch.Tensor | None = None,
+             lse: torch.Tensor | None = None):
+    """softmax(scale * Q K^T) V for bf16 Q [B,Hq,S,D], K/V [B,Hkv,S,D] (contiguous).
+
+    Returns (O bf16 [B,Hq,S,D], lse fp32 [B,Hq,S]); lse is the natural log."""
+    _require(q.dim() == 4 and k.dim() == 4 and v.shape == k.shape, "expected [B,H,S,D] tensors")
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    _require(k.shape[0] == B and k.shape[2] == S and k.shape[3] == D, "K/V shape mismatch")
+    for t in (q, k, v):
+        _require(t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous(),
+                 "q, k, v must be contiguous bf16 CUDA tensors")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    _require(out.shape == q.shape and out.dtype == torch.bfloat16 and out.is_contiguous(), "bad out")
+    _require(lse.shape == (B, Hq, S) and lse.dtype == torch.float32 and lse.is_contiguous(), "bad lse")
+    st = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                      B, Hq, Hkv, S, D, int(bool(causal)), scale, _stream_handle(q.device))
+    _check(st, "attn_fwd")
+    return out, lse
+
+
+def attn_partial(q: torch.Tensor, k_chunk: torch.Tensor, v_chunk: torch.Tensor, q_off: int = 0,
+                 kv_off: int = 0, causal: bool = False, scale: float | None = None,
+                 out: torch.Tensor | None = None, lse: torch.Tensor | None = None):
+    """Attention of Q [B,Hq,Sq,D] against one K/V chunk [B,Hkv,Skv,D].
+
+    The chunk may be a slice along S of a larger contiguous K/V (no copy).
+    q_off / kv_off are the global positions of query row 0 and key 0.
+    Returns (O_i fp32 [B,Hq,Sq,D] normalised within the chunk, lse_i fp32 [B,Hq,Sq])."""
+    _require(q.dim() == 4 and k_chunk.dim() == 4 and v_chunk.shape == k_chunk.shape,
+             "expected [B,H,S,D] tensors")
+    B, Hq, Sq, D = q.shape
+    Hkv, Skv = k_chunk.shape[1], k_chunk.shape[2]
+    _require(k_chunk.shape[0] == B and k_chunk.shape[3] == D, "K/V shape mismatch")
+    _require(q.dtype == torch.bfloat16 and q.is_cuda and q.is_contiguous(), "q must be contiguous bf16")
+    for t in (k_chunk, v_chunk):
+        _require(t.dtype == torch.bfloat16 and t.is_cuda and _rows_contiguous(t),
+                 "k/v chunks must be bf16 with packed rows (a contiguous tensor or an S-slice of one)")
+    _require(k_chunk.stride() == v_chunk.stride(), "k and v chunks must share strides")
+    head_stride = k_chunk.stride(1) if Hkv > 1 or B > 1 else Skv * D
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty((B, Hq, Sq, D), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    _require(out.shape == (B, Hq, Sq, D) and out.dtype == torch.float32 and out.is_contiguous(), "bad out")
+    _require(lse.shape == (B, Hq, Sq) and lse.dtype == torch.float32 and lse.is_contiguous(), "bad lse")
+    st = lib.attn_partial(q.data_ptr(), k_chunk.data_ptr(), v_chunk.data_ptr(), int(q_off), int(kv_off),
+                          int(head_stride), out.data_ptr(), lse.data_ptr(), B, Hq, Hkv, Sq, Skv, D,
+                          int(bool(causal)), scale, _stream_handle(q.device))
+    _check(st, "attn_partial")
+    return out, lse
+
+
+def lse_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, out_dtype=torch.bfloat16,
+              out: torch.Tensor | None = None, lse: torch.Tensor | None = None):
+    """Merge P partials: o_parts fp32 [P,B,H,S,D], lse_parts fp32 [P,B,H,S] -> (O, lse)."""
+    _require(o_parts.dim() == 5 and lse_parts.shape == o_parts.shape[:4], "expected [P,B,H,S,D] and [P,B,H,S]")
+    P, B, H, S, D = o_parts.shape
+    for t in (o_parts, lse_parts):
+        _require(t.dtype == torch.float32 and t.is_cuda and t.is_contiguous(), "partials must be contiguous fp32 CUDA")
+    _require(out_dtype in (torch.bfloat16, torch.float32), "out_dtype must be bf16 or fp32")
+    if out is None:
+        out = torch.empty((B, H, S, D), dtype=out_dtype, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=o_parts.device)
+    _require(out.shape == (B, H, S, D) and out.dtype == out_dtype and out.is_contiguous(), "bad out")
+    _require(lse.shape == (B, H, S) and lse.dtype == torch.float32 and lse.is_contiguous(), "bad lse")
+    st = lib.lse_merge(o_parts.data_ptr(), lse_parts.data_ptr(), P, out.data_ptr(),
+                       ATTN_BF16 if out_dtype == torch.bfloat16 else ATTN_F32, lse.data_ptr(),
+                       B, H, S, D, _stream_handle(o_parts.device))
+    _check(st, "lse_merge")
+    return out, lse
+
+
+def ring_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, causal: bool = False,
+                  scale: float | None = None, o_parts: torch.Tensor | None = None,
+                  lse_parts: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                  lse: torch.Tensor | None = None):
+    """Ring-Attention's per-device arithmetic on one GPU: the keys are split into
+    P equal chunks (S % P == 0); chunk j is attended by attn_partial at kv_off =
+    j*S/P (a zero-copy view), then the P partials are merged by lse_merge.
+    o_parts / lse_parts are optional preallocated fp32 [P,B,Hq,S,D] / [P,B,Hq,S]."""
+    B, Hq, S, D = q.shape
+    _require(P >= 1 and S % P == 0, "S must be a multiple of P")
+    C = S // P
+    if o_parts is None:
+        o_parts = torch.empty((P, B, Hq, S, D), dtype=torch.float32, device=q.device)
+    if lse_parts is None:
+        lse_parts = torch.empty((P, B, Hq, S), dtype=torch.float32, device=q.device)
+    for j in range(P):
+        attn_partial(q, k[:, :, j * C:(j + 1) * C], v[:, :, j * C:(j + 1) * C], 0, j * C, causal, scale,
+                     out=o_parts[j], lse=lse_parts[j])
+    return lse_merge(o_parts, lse_parts, torch.bfloat16, out=out, lse=lse)
+
+
+def query_device_error(device: torch.device | None = None) -> None:
+    """Synchronise the current stream and raise AttnError if a kernel timed out."""
+    device = device or torch.device("cuda", torch.cuda.current_device())
+    _check(lib.attn_query_device_error(_stream_handle(device)), "device wait")

@@ -1,0 +1,50 @@
+"""Loads libseqattn.so (built in-tree by sequence_attn_fwd_gb300.build) via ctypes.
+
+The library must exist: there is no fallback implementation. Import fails
+with a message naming the build command when it is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libseqattn.so")
+
+# Every function the public header include/seqattn.h declares.
+EXPORTS = ["attn_fwd", "attn_partial", "lse_merge", "attn_query_device_error",
+           "attn_status_string", "attn_last_cuda_error"]
+
+STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
+          3: "ATTN_ERR_CUDA", 4: "ATTN_ERR_TIMEOUT"}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        name = STATUS.get(status, str(status))
+        detail = lib.attn_status_string(status).decode() if lib is not None else ""
+        extra = f" (cudaError {lib.attn_last_cuda_error()})" if status == 3 and lib is not None else ""
+        super().__init__(f"{what}: {name}: {detail}{extra}")
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing; build it with `python -m sequence_attn_fwd_gb300.build`")
+    L = ctypes.CDLL(path)
+    P, I, LL, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_float
+    L.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P]
+    L.attn_partial.argtypes = [P, P, P, LL, LL, LL, P, P, I, I, I, I, I, I, I, F, P]
+    L.lse_merge.argtypes = [P, P, I, P, I, P, I, I, I, I, P]
+    L.attn_query_device_error.argtypes = [P]
+    L.attn_status_string.argtypes = [I]
+    L.attn_status_string.restype = ctypes.c_char_p
+    L.attn_last_cuda_error.argtypes = []
+    for name in ("attn_fwd", "attn_partial", "lse_merge", "attn_query_device_error",
+                 "attn_last_cuda_error"):
+        getattr(L, name).restype = ctypes.c_int
+    return L
+
+
+lib = None
+lib = load()

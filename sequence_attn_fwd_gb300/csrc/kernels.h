@@ -1,0 +1,32 @@
+// Host-side interface between the C-ABI layer (api.cu) and the kernel
+// translation units. Not part of the public ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace seqattn {
+
+// Parameters of one attention launch (attn_fwd or attn_partial).
+struct AttnParams {
+  void *o;            // [B, Hq, Sq, D] bf16 (attn_fwd) or fp32 (attn_partial)
+  float *lse;         // [B, Hq, Sq]
+  int B, Hq, Hkv, Sq, Skv;
+  long long q_off, kv_off;  // global positions of query row 0 and key 0
+  float scale_log2;   // softmax scale times log2(e)
+  int causal;
+  int n_qblocks;      // ceil(Sq / 256): two 128-row query tiles per CTA
+};
+
+// Tensor maps are 3-D views [heads][rows][D] of bf16 data, box 64 x 128 x 1,
+// 128-byte swizzle; built by the caller.
+cudaError_t launch_attention(int D, bool f32_out, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                             const CUtensorMap &tm_v, const AttnParams &p, cudaStream_t stream);
+
+cudaError_t launch_lse_merge(const float *o_parts, const float *lse_parts, int P, long long nrows,
+                             int D, void *o, bool bf16_out, float *lse, cudaStream_t stream);
+
+// Reads and clears the device error word (after the caller synchronised).
+cudaError_t read_and_clear_device_error(int *code);
+
+}  // namespace seqattn

@@ -1,0 +1,96 @@
+"""The C-ABI library builds, loads, exports what include/seqattn.h declares and
+rejects bad arguments on the host, before any CUDA call (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sequence_attn_fwd_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "seqattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = build_mod.build()
+    from sequence_attn_fwd_gb300._lib import load
+
+    return load(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    assert declared_functions() == sorted(["attn_fwd", "attn_partial", "lse_merge", "attn_query_device_error",
+                                           "attn_status_string", "attn_last_cuda_error"])
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    from sequence_attn_fwd_gb300._lib import EXPORTS
+
+    assert sorted(EXPORTS) == declared_functions()
+
+
+def test_library_is_built_for_sm103a():
+    log = open(os.path.join(os.path.dirname(build_mod.LIB), "ptxas.log")).read()
+    assert "for 'sm_103a'" in log and "attn_fwd_kernel" in log and "lse_merge_kernel" in log
+    assert "tcgen05" in open(os.path.join(build_mod.CSRC, "ptx.cuh")).read()
+
+
+def test_status_strings(lib):
+    assert lib.attn_status_string(0) == b"ok"
+    assert lib.attn_status_string(4) == b"device-side wait timed out"
+    assert lib.attn_status_string(99) == b"unknown status"
+    assert lib.attn_last_cuda_error() == 0
+
+
+FAKE = 1 << 20  # a 16-byte-aligned non-null address; never dereferenced on these paths
+
+
+def fwd(lib, q=FAKE, B=1, Hq=2, Hkv=2, S=16, D=64, causal=0, scale=0.125):
+    return lib.attn_fwd(q, FAKE, FAKE, FAKE, FAKE, B, Hq, Hkv, S, D, causal, ctypes.c_float(scale), None)
+
+
+def test_attn_fwd_argument_checks(lib):
+    assert fwd(lib, Hq=3, Hkv=2) == 1  # Hq % Hkv != 0
+    assert fwd(lib, D=96) == 2  # unsupported head dim
+    assert fwd(lib, D=256) == 2
+    assert fwd(lib, q=0) == 1  # null pointer
+    assert fwd(lib, q=FAKE + 8) == 1  # misaligned
+    assert fwd(lib, scale=0.0) == 1 and fwd(lib, scale=float("nan")) == 1 and fwd(lib, scale=-1.0) == 1
+    assert fwd(lib, causal=2) == 1
+    assert fwd(lib, B=-1) == 1 and fwd(lib, S=-5) == 1 and fwd(lib, Hkv=0) == 1
+    assert fwd(lib, B=0) == 0 and fwd(lib, S=0) == 0  # empty problems are no-ops
+    assert fwd(lib, q=0, S=0) == 0
+
+
+def test_attn_partial_argument_checks(lib):
+    def part(kv_head_stride=0, Sq=16, Skv=16, D=64, o=FAKE):
+        return lib.attn_partial(FAKE, FAKE, FAKE, 0, 0, kv_head_stride, o, FAKE, 1, 2, 1, Sq, Skv, D, 1,
+                                ctypes.c_float(0.125), None)
+
+    assert part(kv_head_stride=16 * 64 - 8) == 1  # stride shorter than a head
+    assert part(kv_head_stride=16 * 64 + 4) == 1  # not a multiple of 8 elements
+    assert part(o=FAKE + 4) == 1
+    assert part(D=32) == 2
+    assert part(Sq=0) == 0
+
+
+def test_lse_merge_argument_checks(lib):
+    def merge(P=2, o_dtype=0, D=128, S=8, parts=FAKE):
+        return lib.lse_merge(parts, FAKE, P, FAKE, o_dtype, FAKE, 1, 2, S, D, None)
+
+    assert merge(P=0) == 1
+    assert merge(o_dtype=7) == 1
+    assert merge(D=80) == 2
+    assert merge(parts=0) == 1
+    assert merge(parts=FAKE + 4) == 1
+    assert merge(S=0) == 0

@@ -1,0 +1,203 @@
+"""CUDA path vs the fp64 oracle, element by element, through the C ABI.
+
+Small cases span several 128-row tiles and a ragged tail and are checked in
+full; the five named workloads run at full size in the launch configuration
+the benchmark times and are checked on sampled query rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests.parity import LSE_TOL, O_TOL, check_lse, check_o, gather_rows
+
+pytestmark = pytest.mark.gpu
+
+W = workloads.WORKLOADS
+
+
+@pytest.fixture(scope="module")
+def sa(cuda_dev):
+    import sequence_attn_fwd_gb300 as sa
+
+    yield sa
+    sa.query_device_error()  # no kernel may have recorded a timed-out wait
+
+
+def adhoc(B, Hq, Hkv, S, D, causal, seed=77):
+    return workloads.Workload("adhoc", B, Hq, Hkv, S, D, causal, 1, seed)
+
+
+def to_dev(*ts):
+    return [t.cuda() for t in ts]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_tiny_workload_full(sa, causal):
+    w = W["tiny_b1h2s256d64"]
+    q, k, v = workloads.make_qkv(w)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal)
+    o, lse = sa.attn_fwd(*to_dev(q, k, v), causal=causal)
+    check_o(o, o_ref)
+    check_lse(lse, lse_ref)
+
+
+def test_tiny_workload_matches_stored_golden_rows(sa):
+    from tests.test_golden import load_golden
+
+    g, cases = load_golden()
+    w = W[g["workload"]]
+    q, k, v = workloads.make_qkv(w)
+    for name, (o_ref, lse_ref) in cases.items():
+        o, lse = sa.attn_fwd(*to_dev(q, k, v), causal=(name == "causal"))
+        check_o(o[0, :, g["rows"]], o_ref)
+        check_lse(lse[0, :, g["rows"]], lse_ref)
+
+
+SHAPES = [
+    # B, Hq, Hkv, S, D, causal
+    (2, 4, 2, 1000, 128, True),
+    (2, 4, 2, 1000, 128, False),
+    (1, 3, 1, 777, 64, True),
+    (1, 6, 3, 640, 64, False),
+    (1, 2, 1, 129, 128, True),
+    (1, 2, 2, 127, 64, False),
+    (1, 1, 1, 1, 128, True),
+    (1, 1, 1, 1, 64, False),
+    (3, 2, 2, 384, 128, True),
+    (1, 8, 1, 520, 128, True),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "b{}hq{}hkv{}s{}d{}{}".format(*s[:5], "c" if s[5] else ""))
+def test_attn_fwd_against_oracle(sa, shape):
+    B, Hq, Hkv, S, D, causal = shape
+    q, k, v = workloads.make_qkv(adhoc(B, Hq, Hkv, S, D, causal))
+    o_ref, lse_ref = oracle.attention(q, k, v, causal)
+    o, lse = sa.attn_fwd(*to_dev(q, k, v), causal=causal)
+    check_o(o, o_ref)
+    check_lse(lse, lse_ref)
+
+
+def test_attn_fwd_custom_scale_and_large_scores(sa):
+    """Scores of a few hundred: exponentials stay finite only with the max subtracted."""
+    q, k, v = workloads.make_qkv(adhoc(1, 2, 2, 300, 128, True, seed=5))
+    q = (q.float() * 8).to(torch.bfloat16)
+    o_ref, lse_ref = oracle.attention(q, k, v, True, scale=0.5)
+    o, lse = sa.attn_fwd(*to_dev(q, k, v), causal=True, scale=0.5)
+    check_o(o, o_ref)
+    check_lse(lse, lse_ref)
+
+
+def test_outputs_leave_neighbouring_memory_untouched(sa):
+    """Guard regions around every output (compute-sanitizer stands in for nothing here)."""
+    B, Hq, S, D = 1, 3, 333, 128
+    q, k, v = to_dev(*workloads.make_qkv(adhoc(B, Hq, Hq, S, D, True)))
+    n_o, n_l, g = B * Hq * S * D, B * Hq * S, 4096
+    o_buf = torch.full((n_o + 2 * g,), 7.0, dtype=torch.bfloat16, device="cuda")
+    l_buf = torch.full((n_l + 2 * g,), 7.0, dtype=torch.float32, device="cuda")
+    o = o_buf[g:g + n_o].view(B, Hq, S, D)
+    lse = l_buf[g:g + n_l].view(B, Hq, S)
+    sa.attn_fwd(q, k, v, causal=True, out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert (o_buf[:g] == 7).all() and (o_buf[g + n_o:] == 7).all()
+    assert (l_buf[:g] == 7).all() and (l_buf[g + n_l:] == 7).all()
+    po = torch.full((n_o + 2 * g,), 7.0, dtype=torch.float32, device="cuda")
+    sa.attn_partial(q, k[:, :, 100:200], v[:, :, 100:200], 0, 100, True,
+                    out=po[g:g + n_o].view(B, Hq, S, D), lse=l_buf[g:g + n_l].view(B, Hq, S))
+    torch.cuda.synchronize()
+    assert (po[:g] == 7).all() and (po[g + n_o:] == 7).all()
+    assert (l_buf[:g] == 7).all() and (l_buf[g + n_l:] == 7).all()
+
+
+@pytest.mark.parametrize("q_off,a,b", [(0, 0, 256), (0, 256, 700), (0, 700, 1000), (300, 128, 512), (0, 999, 1000)])
+def test_attn_partial_offsets_against_oracle(sa, q_off, a, b):
+    B, Hq, Hkv, S, D = 1, 4, 2, 1000, 128
+    q, k, v = workloads.make_qkv(adhoc(B, Hq, Hkv, S, D, True, seed=9))
+    qb = q[:, :, q_off:].contiguous()
+    o_ref, lse_ref = oracle.attention(qb, k[:, :, a:b].contiguous(), v[:, :, a:b].contiguous(), True,
+                                      q_off=q_off, kv_off=a)
+    qd, kd, vd = to_dev(qb, k, v)
+    o, lse = sa.attn_partial(qd, kd[:, :, a:b], vd[:, :, a:b], q_off, a, True)
+    check_o(o, o_ref, bf16_out=False)
+    check_lse(lse, lse_ref)
+
+
+def test_attn_partial_chunk_invisible_to_every_row(sa):
+    q, k, v = to_dev(*workloads.make_qkv(adhoc(1, 2, 2, 512, 64, True)))
+    o, lse = sa.attn_partial(q[:, :, :256].contiguous(), k[:, :, 256:], v[:, :, 256:], 0, 256, True)
+    torch.cuda.synchronize()
+    assert (o == 0).all() and torch.isneginf(lse).all()
+
+
+def test_ring_reduced_size_against_oracle_and_single_pass(sa):
+    w = W["ring8_b2h32s4096d128_causal"]
+    S = 1024
+    q, k, v = workloads.make_qkv(w, S=S)
+    q, k, v = q[:, :4].contiguous(), k[:, :4].contiguous(), v[:, :4].contiguous()
+    o_ref, lse_ref = oracle.attention(q, k, v, True)
+    qd, kd, vd = to_dev(q, k, v)
+    o_ring, lse_ring = sa.ring_attn_fwd(qd, kd, vd, P=8, causal=True)
+    check_o(o_ring, o_ref)
+    check_lse(lse_ring, lse_ref)
+    o_one, lse_one = sa.attn_fwd(qd, kd, vd, causal=True)
+    assert (o_ring.float() - o_one.float()).abs().max().item() <= O_TOL
+    assert (lse_ring - lse_one).abs().max().item() <= LSE_TOL
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal_pattern", [True, False])
+def test_lse_merge_on_synthetic_partials(sa, D, causal_pattern):
+    P, B, H, S = 16, 2, 3, 512
+    o_parts, lse_parts = workloads.make_partials(P, B, H, S, D, seed=31, causal=causal_pattern)
+    if not causal_pattern:  # scattered empty partials and one fully empty row
+        lse_parts[3, 0, 1, :100] = -np.inf
+        lse_parts[:, 1, 2, 7] = -np.inf
+    o_ref, lse_ref = oracle.lse_merge(o_parts, lse_parts)
+    op, lp = to_dev(o_parts, lse_parts)
+    o32, l32 = sa.lse_merge(op, lp, out_dtype=torch.float32)
+    check_o(o32, o_ref, tol=1e-5, bf16_out=False)
+    check_lse(l32, lse_ref, tol=1e-5)
+    o16, l16 = sa.lse_merge(op, lp, out_dtype=torch.bfloat16)
+    check_o(o16, o_ref, tol=O_TOL)
+    # in place: the merged result written over part 0
+    sa.lse_merge(op, lp, out_dtype=torch.float32, out=op[0], lse=lp[0])
+    check_o(op[0], o_ref, tol=1e-5, bf16_out=False)
+    check_lse(lp[0], lse_ref, tol=1e-5)
+
+
+@pytest.mark.parametrize("P", [1, 2, 5, 33])
+def test_lse_merge_part_counts(sa, P):
+    o_parts, lse_parts = workloads.make_partials(P, 1, 2, 130, 128, seed=40 + P, causal=False)
+    o_ref, lse_ref = oracle.lse_merge(o_parts, lse_parts)
+    o, l = sa.lse_merge(*to_dev(o_parts, lse_parts), out_dtype=torch.float32)
+    check_o(o, o_ref, tol=1e-5, bf16_out=False)
+    check_lse(l, lse_ref, tol=1e-5)
+
+
+# ----------------------------------------------------------------- full-size workloads
+
+def run_workload(sa, w, q, k, v):
+    """The launch configuration the benchmark times for this workload."""
+    if w.P == 1:
+        return sa.attn_fwd(q, k, v, causal=w.causal)
+    return sa.ring_attn_fwd(q, k, v, P=w.P, causal=w.causal)
+
+
+@pytest.mark.parametrize("name", list(W))
+def test_full_size_workload_sampled_rows(sa, name):
+    w = W[name]
+    q, k, v = workloads.make_qkv(w)
+    rows = workloads.sample_query_rows(w, n=w.sample_rows or 32)
+    # chunk boundaries and the last row are checked too
+    extra = np.array(sorted({0, w.chunk - 1, w.chunk, w.S - 1} & set(range(w.S))), dtype=np.int64)
+    rows = np.sort(np.concatenate([rows, np.tile(extra, (rows.shape[0], 1))], axis=1), axis=1)
+    o_ref, lse_ref = oracle.attention(q, k, v, w.causal, rows=rows)
+    qd, kd, vd = to_dev(q, k, v)
+    del q, k, v
+    o, lse = run_workload(sa, w, qd, kd, vd)
+    check_o(gather_rows(o, rows), o_ref)
+    check_lse(gather_rows(lse, rows), lse_ref)
+    del o, lse, qd, kd, vd
+    torch.cuda.empty_cache()

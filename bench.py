@@ -194,8 +194,8 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int):
 
     F = w.attention_flops()
     sampler = ClockSampler(dev.index) if rank == 0 else None
-    # warm-up: at least W steps and about a second of work so clocks settle
-    t_end = time.time() + 1.0
+    # warm-up: at least W steps and --warmup-seconds of work so clocks settle
+    t_end = time.time() + args.warmup_seconds
     n = 0
     while n < args.warmup or time.time() < t_end:
         step(q, k, v)
@@ -343,6 +343,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--warmup-seconds", type=float, default=1.0)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--reference-budget", type=float, default=3.0, help="CPU seconds per reference step")
     ap.add_argument("--cpu-baseline-budget", type=float, default=15.0)

@@ -30,7 +30,7 @@ class AttnError(RuntimeError):
 
 def load(path: str = LIB_PATH) -> ctypes.CDLL:
     if not os.path.exists(path):
-        raise ImportError(f"{path} is missing; build it with `python -m sequence_attn_fwd_gb300.build`")
+        raise ImportError(f"{path} is missing; build it with `python sequence_attn_fwd_gb300/build.py`")
     L = ctypes.CDLL(path)
     P, I, LL, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_float
     L.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P]

@@ -1,6 +1,9 @@
 """Builds libseqattn.so in-tree with nvcc for sm_103a (GB300).
 
-    python -m sequence_attn_fwd_gb300.build [--force]
+    python sequence_attn_fwd_gb300/build.py [--force]
+
+(run as a script: importing the package loads the library, so the build
+cannot go through the package import).
 
 Each translation unit is compiled in parallel, then linked into
 ``sequence_attn_fwd_gb300/lib/libseqattn.so`` (the CUDA runtime is linked

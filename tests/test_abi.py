@@ -6,7 +6,9 @@ import re
 
 import pytest
 
-from sequence_attn_fwd_gb300 import build as build_mod
+from __graft_entry__ import _build_module
+
+build_mod = _build_module()
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "seqattn.h")

@@ -116,6 +116,36 @@ const char *attn_status_string(int status);
 /* The cudaError_t of the most recent ATTN_ERR_CUDA (0 if none). */
 int attn_last_cuda_error(void);
 
+/* Size of the library's fixed scratch array used by attn_ring_fwd_static. */
+#define SEQATTN_RING_SCRATCH_BYTES (64ull << 20) /* 64 MiB */
+
+/*
+ * attn_ring_fwd_static -- the ring-emulated forward (keys split into P equal
+ * chunks, one attn_partial per chunk, then lse_merge into bf16 o and fp32 lse),
+ * with the fp32 partials kept in a fixed device array owned by the library
+ * instead of in memory the caller provides. The source pages have no
+ * counterpart to this entry point; it exists for callers that must not or
+ * cannot allocate device memory themselves: code inside a host application
+ * whose allocator already holds nearly all device memory, or latency-sensitive
+ * loops that cannot afford cudaMalloc/cudaFree (which may synchronise the
+ * device). It allocates nothing.
+ *
+ *   q  bf16 [B, Hq, S, D]; k, v bf16 [B, Hkv, S, D]; o bf16 [B, Hq, S, D];
+ *   lse fp32 [B, Hq, S]. S % P == 0. Other rules as attn_fwd.
+ *   Limit: P * B * Hq * S * (D + 1) * 4 bytes (each part rounded up to 256 B)
+ *   must fit in SEQATTN_RING_SCRATCH_BYTES; larger problems are rejected with
+ *   ATTN_ERR_UNSUPPORTED before anything is launched.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any stream
+ *   capture on the device. Every call on a device shares the one array: calls
+ *   whose kernels overlap on the GPU (different streams, no ordering between
+ *   them) race on it and give wrong results. Each call writes every partial
+ *   element it reads, so the contents left by an earlier call do no harm.
+ */
+int attn_ring_fwd_static(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                         int Hq, int Hkv, int S, int D, int P, int causal, float scale,
+                         attn_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -19,8 +19,10 @@ import torch
 
 from ._lib import AttnError, lib
 
-__all__ = ["attn_fwd", "attn_partial", "lse_merge", "ring_attn_fwd", "query_device_error",
-           "AttnError", "lib"]
+__all__ = ["attn_fwd", "attn_partial", "lse_merge", "ring_attn_fwd", "ring_attn_fwd_static",
+           "query_device_error", "AttnError", "lib", "RING_SCRATCH_BYTES"]
+
+RING_SCRATCH_BYTES = 64 << 20  # the library's fixed scratch array for ring_attn_fwd_static
 
 ATTN_BF16, ATTN_F32 = 0, 1
 
@@ -146,6 +148,34 @@ def ring_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, cau
         attn_partial(q, k[:, :, j * C:(j + 1) * C], v[:, :, j * C:(j + 1) * C], 0, j * C, causal, scale,
                      out=o_parts[j], lse=lse_parts[j])
     return lse_merge(o_parts, lse_parts, torch.bfloat16, out=out, lse=lse)
+
+
+def ring_attn_fwd_static(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, causal: bool = False,
+                         scale: float | None = None, out: torch.Tensor | None = None,
+                         lse: torch.Tensor | None = None):
+    """ring_attn_fwd without caller-side scratch: the fp32 partials live in a
+    fixed 64 MiB device array inside the library (attn_ring_fwd_static), so
+    the C call itself allocates nothing. Meant for callers that cannot allocate
+    device memory (a host application whose allocator owns the device memory,
+    or loops that cannot afford cudaMalloc/cudaFree). Problems whose partials
+    exceed the array are rejected. Calls that overlap on the GPU share the
+    array and race; the first call on a device sets up the array's address.
+    Here ``out``/``lse`` are allocated through torch only when not given."""
+    _require(q.dim() == 4 and k.dim() == 4 and v.shape == k.shape, "expected [B,H,S,D] tensors")
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    for t in (q, k, v):
+        _require(t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous(),
+                 "q, k, v must be contiguous bf16 CUDA tensors")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    st = lib.attn_ring_fwd_static(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                  B, Hq, Hkv, S, D, int(P), int(bool(causal)), scale, _stream_handle(q.device))
+    _check(st, "attn_ring_fwd_static")
+    return out, lse
 
 
 def query_device_error(device: torch.device | None = None) -> None:

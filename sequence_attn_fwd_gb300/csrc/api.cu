@@ -166,3 +166,80 @@ const char *attn_status_string(int status) {
 int attn_last_cuda_error(void) { return g_last_cuda_error.load(); }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Ring forward with library-owned scratch, for callers that cannot allocate.
+//
+// Some callers of this library must not, or cannot, call cudaMalloc: code
+// embedded in a host application whose own allocator has already reserved
+// nearly all device memory (a raw allocation would fail or fragment it), and
+// latency-sensitive loops where cudaMalloc/cudaFree are unacceptable because
+// they can synchronise the whole device. attn_ring_fwd_static serves them: the
+// fp32 per-chunk partials that ring_attn_fwd keeps in caller memory live here
+// in one fixed device array instead. Every GPU that loads this library holds
+// the array (kRingScratchBytes) until the process exits.
+//
+// In host code `g_ring_scratch` is only a host-side stand-in for the device
+// symbol; its device address comes from cudaGetSymbolAddress, looked up once
+// per device (with that device current) on the first call there.
+static __device__ __align__(256) unsigned char g_ring_scratch[SEQATTN_RING_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_ring_scratch_mutex;
+void *g_ring_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (set up on first use).
+int ring_scratch_address(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_ring_scratch_mutex);
+  if (!g_ring_scratch_ptr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_ring_scratch);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_ring_scratch_ptr[dev] = p;
+  }
+  *out = g_ring_scratch_ptr[dev];
+  return ATTN_OK;
+}
+
+size_t align_up_256(size_t n) { return (n + 255u) & ~static_cast<size_t>(255u); }
+
+}  // namespace
+
+extern "C" int attn_ring_fwd_static(const void *q, const void *k, const void *v, void *o,
+                                    float *lse, int B, int Hq, int Hkv, int S, int D, int P,
+                                    int causal, float scale, attn_stream_t stream) {
+  if (P < 1 || S < 0 || B < 0 || Hq <= 0) return ATTN_ERR_INVALID_ARG;
+  if (S % P != 0) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  const long long rows = static_cast<long long>(B) * Hq * S;
+  if (rows == 0) return ATTN_OK;
+  // partials: o_parts fp32 [P, B, Hq, S, D], then lse_parts fp32 [P, B, Hq, S]
+  const size_t o_bytes = align_up_256(static_cast<size_t>(P) * rows * D * sizeof(float));
+  const size_t l_bytes = align_up_256(static_cast<size_t>(P) * rows * sizeof(float));
+  if (o_bytes + l_bytes > static_cast<size_t>(SEQATTN_RING_SCRATCH_BYTES)) return ATTN_ERR_UNSUPPORTED;
+  void *scratch = nullptr;
+  int st = ring_scratch_address(&scratch);
+  if (st != ATTN_OK) return st;
+  float *o_parts = static_cast<float *>(scratch);
+  float *lse_parts = reinterpret_cast<float *>(static_cast<unsigned char *>(scratch) + o_bytes);
+  // Every partial element the merge reads is written by the hops of this same
+  // call (rows a chunk cannot see get O = 0, lse = -inf), so nothing left in
+  // the array by an earlier call needs clearing.
+  const int C = S / P;
+  for (int j = 0; j < P; ++j) {
+    const size_t kv_offset = static_cast<size_t>(j) * C * D;  // elements: chunk j of every head
+    st = attn_partial(q, static_cast<const unsigned char *>(k) + kv_offset * 2,
+                      static_cast<const unsigned char *>(v) + kv_offset * 2, 0,
+                      static_cast<long long>(j) * C, static_cast<long long>(S) * D,
+                      o_parts + static_cast<size_t>(j) * rows * D, lse_parts + static_cast<size_t>(j) * rows,
+                      B, Hq, Hkv, S, C, D, causal, scale, stream);
+    if (st != ATTN_OK) return st;
+  }
+  return lse_merge(o_parts, lse_parts, P, o, ATTN_BF16, lse, B, Hq, S, D, stream);
+}

@@ -30,7 +30,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted(["attn_fwd", "attn_partial", "lse_merge", "attn_query_device_error",
-                                           "attn_status_string", "attn_last_cuda_error"])
+                                           "attn_status_string", "attn_last_cuda_error",
+                                           "attn_ring_fwd_static"])
 
 
 def test_library_exports_every_declared_symbol(lib):

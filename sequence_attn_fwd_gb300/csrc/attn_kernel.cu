@@ -51,7 +51,7 @@ template <int D>
 struct Cfg {
   static constexpr int kColBlocks = D / 64;
   static constexpr int kTileBytes = kRowsPerTile * D * 2;
-  static constexpr int kStages = (D == 128) ? 4 : 6;
+  static constexpr int kStages = (D == 128) ? 4 : 8;
   static constexpr int kSmemQ = 2 * kTileBytes;
   static constexpr int kSmemRing = kStages * kTileBytes;
   // barriers: q, full[S], empty[S], s_full[2], p_full[2], o_full[2], mma_done
@@ -70,6 +70,56 @@ __device__ __forceinline__ int kv_tiles_for(const AttnParams &p, int first_row) 
   if (max_key < 0) return 0;
   const long long n = max_key / kRowsPerTile + 1;
   return n < n_all ? static_cast<int>(n) : n_all;
+}
+
+// Maximum of the 128 scores of a row (raw, before scaling).
+__device__ __forceinline__ float row_max(const float *s) {
+  float a = s[0], b = s[1], c = s[2], d = s[3];
+#pragma unroll
+  for (int i = 4; i < 124; i += 8) {
+    a = fmax3(a, s[i], s[i + 1]);
+    b = fmax3(b, s[i + 2], s[i + 3]);
+    c = fmax3(c, s[i + 4], s[i + 5]);
+    d = fmax3(d, s[i + 6], s[i + 7]);
+  }
+  a = fmax3(a, s[124], s[125]);
+  b = fmax3(b, s[126], s[127]);
+  return fmax3(fmaxf(a, b), c, d);
+}
+
+// P = 2^(s * c2 - m_ref) for the 128 scores of a row, packed as bf16 pairs
+// (element 2i in the low half), returning the fp32 sum of the unrounded P.
+// With kTrackMax the raw row maximum is found in the same pass.
+template <bool kTrackMax>
+__device__ __forceinline__ float exp_row(const float *s, float c2, float m_ref, uint32_t *pk,
+                                         float *mx_out) {
+  const uint64_t scale2 = f2_pack(c2, c2);
+  const uint64_t neg_m2 = f2_pack(-m_ref, -m_ref);
+  uint64_t sum_a = f2_pack(0.f, 0.f), sum_b = sum_a;
+  float ma = -INFINITY, mb = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < 64; c += 2) {
+    float x0, x1, x2, x3;
+    f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), scale2, neg_m2), x0, x1);
+    f2_unpack(f2_fma(f2_pack(s[2 * c + 2], s[2 * c + 3]), scale2, neg_m2), x2, x3);
+    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+    const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+    sum_a = f2_add(sum_a, f2_pack(p0, p1));
+    sum_b = f2_add(sum_b, f2_pack(p2, p3));
+    if (kTrackMax) {
+      ma = fmax3(ma, s[2 * c], s[2 * c + 1]);
+      mb = fmax3(mb, s[2 * c + 2], s[2 * c + 3]);
+    }
+    __nv_bfloat162 h0 = __floats2bfloat162_rn(p0, p1);
+    __nv_bfloat162 h1 = __floats2bfloat162_rn(p2, p3);
+    pk[c] = *reinterpret_cast<uint32_t *>(&h0);
+    pk[c + 1] = *reinterpret_cast<uint32_t *>(&h1);
+  }
+  if (kTrackMax) *mx_out = fmaxf(ma, mb);
+  float a0, a1, b0, b1;
+  f2_unpack(sum_a, a0, a1);
+  f2_unpack(sum_b, b0, b1);
+  return (a0 + a1) + (b0 + b1);
 }
 
 template <int D, bool kF32Out>
@@ -179,19 +229,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_base = smem_addr(sQ);
       const uint32_t ring_base = smem_addr(sRing);
       bool ok = n_max > 0 && mbar_wait(bar(kBarQ), 0, abort_flag, err);
+      // Per KV step j: PV_0(j-1), S_0(j), PV_1(j-1), S_1(j). Both ring slots of
+      // the step are waited for first (measured faster on GB300 than waiting
+      // for each just before its first use); each slot is released by a commit
+      // that fires when its last MMA completes.
       for (int j = 0; ok && j <= n_max; ++j) {
         const int cK = 2 * j, cV = 2 * j - 1;  // ring positions of K_j and V_{j-1}
-        if (j < n_max && !mbar_wait(bar(kBarFull + cK % C::kStages), (cK / C::kStages) & 1,
-                                    abort_flag, err))
-          break;
-        if (j >= 1 && !mbar_wait(bar(kBarFull + cV % C::kStages), (cV / C::kStages) & 1,
-                                 abort_flag, err))
-          break;
+        const int sK = cK % C::kStages, sV = (cV + C::kStages) % C::kStages;
+        const uint32_t k_base = ring_base + sK * C::kTileBytes;
+        const uint32_t v_base = ring_base + sV * C::kTileBytes;
+        if (j < n_max && !mbar_wait(bar(kBarFull + sK), (cK / C::kStages) & 1, abort_flag, err)) break;
+        if (j >= 1 && !mbar_wait(bar(kBarFull + sV), (cV / C::kStages) & 1, abort_flag, err)) break;
         tc_fence_after();
-        const uint32_t k_base = ring_base + (cK % C::kStages) * C::kTileBytes;
-        const uint32_t v_base = ring_base + ((cV + C::kStages) % C::kStages) * C::kTileBytes;
         for (int t = 0; t < 2 && ok; ++t) {
-          if (j >= 1 && j - 1 < n_tiles[t]) {
+          const int nt = t ? n_tiles[1] : n_tiles[0];
+          if (j >= 1 && j - 1 < nt) {
             // O_t += P_t V_{j-1}; P_t was written over S_t by the softmax warps
             if (!mbar_wait(bar(kBarPFull + t), (j - 1) & 1, abort_flag, err)) {
               ok = false;
@@ -203,9 +255,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t bdesc = sw128_desc(v_base + kk * 2048, kColBlockBytes, 1024);
               mma_ts(tO(t), tS(t) + kk * 8, bdesc, idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
             }
-            if (j - 1 == n_tiles[t] - 1) mma_commit(bar(kBarOFull + t));
+            if (j - 1 == nt - 1) mma_commit(bar(kBarOFull + t));
+            if (t == 1 || j - 1 >= n_tiles[1]) mma_commit(bar(kBarEmpty + sV));  // last use of V_{j-1}
           }
-          if (j < n_tiles[t]) {
+          if (j < nt) {
             // S_t = Q_t K_j^T
             const uint32_t qt = q_base + t * C::kTileBytes;
 #pragma unroll
@@ -215,11 +268,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                      idesc_s, kk > 0 ? 1u : 0u);
             }
             mma_commit(bar(kBarSFull + t));
+            if (t == 1 || j >= n_tiles[1]) mma_commit(bar(kBarEmpty + sK));  // last use of K_j
           }
         }
-        if (!ok) break;
-        if (j >= 1) mma_commit(bar(kBarEmpty + (cV % C::kStages)));
-        if (j < n_max) mma_commit(bar(kBarEmpty + (cK % C::kStages)));
       }
       // All MMAs issued here must be complete before TMEM is released.
       mma_commit(bar(kBarMmaDone));
@@ -240,46 +291,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float c2 = p.scale_log2;
     float m = -INFINITY;  // running max of scale*log2(e)*s (the reference for P)
     float l = 0.f;        // running sum of P relative to m
+    float m_grow = -INFINITY;  // candidate new reference from the latest tile
     bool ok = true;
 
     for (int j = 0; j < n; ++j) {
       ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull + t), j & 1, abort_flag, err));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[128];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        tmem_ld32(s_addr + 32 * i, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * i]));
-      tmem_ld_wait(sr);
-      float *s = reinterpret_cast<float *>(sr);
-
       const int kv0 = j * kRowsPerTile;
       const bool tail = kv0 + kRowsPerTile > p.Skv;
       const bool diag = p.causal && (p.kv_off + kv0 + kRowsPerTile - 1 > tile_first_q);
+      int last = 127;  // last visible column of this row in the tile
       if (tail || diag) {
-        long long lim = static_cast<long long>(p.Skv) - kv0 - 1;  // last visible column
+        long long lim = static_cast<long long>(p.Skv) - kv0 - 1;
         if (p.causal) {
           const long long c_lim = qpos - p.kv_off - kv0;
           lim = c_lim < lim ? c_lim : lim;
         }
-        const int last = static_cast<int>(lim < -1 ? -1 : (lim > 127 ? 127 : lim));
-#pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c > last) s[c] = -INFINITY;
+        last = static_cast<int>(lim < -1 ? -1 : (lim > 127 ? 127 : lim));
       }
-      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+      // The row of S for this tile, masked (TMEM keeps S until P is written).
+      auto load_scores = [&](uint32_t (&sr)[128]) {
 #pragma unroll
-      for (int c = 4; c < 128; c += 4) {
-        mx0 = fmaxf(mx0, s[c]);
-        mx1 = fmaxf(mx1, s[c + 1]);
-        mx2 = fmaxf(mx2, s[c + 2]);
-        mx3 = fmaxf(mx3, s[c + 3]);
+        for (int i = 0; i < 4; ++i)
+          tmem_ld32(s_addr + 32 * i, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * i]));
+        tmem_ld_wait(sr);
+        if (tail || diag) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c > last) sr[c] = __float_as_uint(-INFINITY);
+        }
+      };
+      uint32_t pk[64];
+      float rowsum;
+      {
+        uint32_t sr[128];
+        load_scores(sr);
+        const float *s = reinterpret_cast<const float *>(sr);
+        if (j == 0) {
+          // no reference yet: the tile maximum first, then the exponentials
+          m = row_max(s) * c2;
+          rowsum = exp_row<false>(s, c2, (m == -INFINITY) ? 0.f : m, pk, nullptr);
+        } else {
+          // Exponentiate against the current reference while finding the tile
+          // maximum; only if some row's maximum grew by more than 2^8 (rare
+          // after the first tiles) is O rescaled and the pass redone.
+          float mx;
+          rowsum = exp_row<true>(s, c2, (m == -INFINITY) ? 0.f : m, pk, &mx);
+          m_grow = fmaxf(m, mx * c2);
+        }
       }
-      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c2;
-      const float m_new = fmaxf(m, m_tile);
-      if (j == 0) {
-        m = m_new;
-      } else {
+      if (j > 0) {
+        const float m_new = m_grow;
         const bool grow = (m_new - m) > kRescaleThreshold;  // false while both are -inf
         if (__any_sync(0xffffffffu, grow)) {
           const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m - m_new);
@@ -298,21 +361,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(o_addr + 32 * cb, orr);
           }
           tmem_st_wait();
+          uint32_t sr[128];
+          load_scores(sr);
+          rowsum = exp_row<false>(reinterpret_cast<const float *>(sr), c2,
+                                  (m == -INFINITY) ? 0.f : m, pk, nullptr);
         }
       }
-      const float m_use = (m == -INFINITY) ? 0.f : m;
-      float sum0 = 0.f, sum1 = 0.f;
-      uint32_t pk[64];
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float p0 = ex2_approx(fmaf(s[2 * c], c2, -m_use));
-        const float p1 = ex2_approx(fmaf(s[2 * c + 1], c2, -m_use));
-        sum0 += p0;
-        sum1 += p1;
-        __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);  // p0 in the low half
-        pk[c] = *reinterpret_cast<uint32_t *>(&h);
-      }
-      l += sum0 + sum1;
+      l += rowsum;
       tmem_st32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
       tmem_st32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
       tmem_st_wait();

@@ -264,7 +264,8 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int):
     achieved = flops_per_launch / (attn_avg_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"], "traffic": None,
-                "kernel": "attn_fwd_kernel<128,f32 out> (attn_partial)" if P > 1 else "attn_fwd_kernel<128,bf16 out>",
+                "kernel": ("attn_fwd_2sm_kernel" if D == 128 and os.environ.get("SEQATTN_ATTN_KERNEL") == "2sm"
+                           else f"attn_fwd_kernel<{D}>") + ("<f32 out> (attn_partial)" if P > 1 else "<bf16 out>"),
                 "peak_source": f"{peak_src} bf16 burst", "launch_ms": attn_avg_ms}
     merge = None
     if merge_ms:

@@ -44,16 +44,16 @@ EncodeTiledFn encode_fn() {
 }
 
 // 3-D bf16 view [heads][rows][D] with the head stride given in elements; box
-// 64 x 128 x 1 with 128-byte swizzle. Rows past `rows` read as zero.
+// 64 x box_rows x 1 with 128-byte swizzle. Rows past `rows` read as zero.
 bool make_map(CUtensorMap *map, const void *base, int D, long long rows, long long heads,
-              long long head_stride) {
+              long long head_stride, unsigned box_rows = 128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
                         static_cast<cuuint64_t>(heads)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2u,
                            static_cast<cuuint64_t>(head_stride) * 2u};
-  cuuint32_t box[3] = {64u, 128u, 1u};
+  cuuint32_t box[3] = {64u, box_rows, 1u};
   cuuint32_t estride[3] = {1u, 1u, 1u};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
             estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -85,10 +85,12 @@ int run_attention(const void *q, const void *k, const void *v, long long q_off, 
     return ATTN_ERR_INVALID_ARG;
 
   CUtensorMap tq, tk, tv;
+  const bool pair = seqattn::attention_uses_pair(D);
   // An empty key set still needs well-formed maps; no KV tile is ever loaded.
   const long long kv_rows = Skv > 0 ? Skv : 1;
   if (!make_map(&tq, q, D, Sq, static_cast<long long>(B) * Hq, static_cast<long long>(Sq) * D) ||
-      !make_map(&tk, k, D, kv_rows, static_cast<long long>(B) * Hkv, kv_head_stride) ||
+      !make_map(&tk, k, D, kv_rows, static_cast<long long>(B) * Hkv, kv_head_stride,
+                pair ? 64u : 128u) ||
       !make_map(&tv, v, D, kv_rows, static_cast<long long>(B) * Hkv, kv_head_stride))
     return cuda_fail(cudaErrorInvalidValue);
 
@@ -105,7 +107,7 @@ int run_attention(const void *q, const void *k, const void *v, long long q_off, 
   p.scale_log2 = scale * 1.4426950408889634f;
   p.causal = causal;
   p.n_qblocks = (Sq + 255) / 256;
-  cudaError_t e = seqattn::launch_attention(D, f32_out, tq, tk, tv, p, stream);
+  cudaError_t e = seqattn::launch_attention(D, f32_out, pair, tq, tk, tv, p, stream);
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 

@@ -1,0 +1,231 @@
+// Pieces shared by the attention kernels: tile counting, the row maximum,
+// the exponent pass, and the softmax + epilogue role of one query row.
+#pragma once
+#include <cuda_bf16.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace seqattn {
+namespace detail {
+
+constexpr int kRowsPerTile = 128;  // MMA M and KV tile length
+constexpr int kColBlockBytes = 128 * 128;  // 128 rows x 128 bytes (64 bf16) swizzle block
+constexpr float kLn2 = 0.693147180559945309f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows > 2^8
+
+// Per-tile number of KV tiles to visit (0 when the tile has no valid row or
+// none of its rows sees any key).
+__device__ __forceinline__ int kv_tiles_for(const AttnParams &p, int first_row) {
+  const int n_all = (p.Skv + kRowsPerTile - 1) / kRowsPerTile;
+  if (first_row >= p.Sq || n_all == 0) return 0;
+  if (!p.causal) return n_all;
+  const int last_row = min(first_row + kRowsPerTile - 1, p.Sq - 1);
+  const long long max_key = p.q_off + last_row - p.kv_off;  // largest visible key index
+  if (max_key < 0) return 0;
+  const long long n = max_key / kRowsPerTile + 1;
+  return n < n_all ? static_cast<int>(n) : n_all;
+}
+
+// Maximum of the 128 scores of a row (raw, before scaling).
+__device__ __forceinline__ float row_max(const float *s) {
+  float a = s[0], b = s[1], c = s[2], d = s[3];
+#pragma unroll
+  for (int i = 4; i < 124; i += 8) {
+    a = fmax3(a, s[i], s[i + 1]);
+    b = fmax3(b, s[i + 2], s[i + 3]);
+    c = fmax3(c, s[i + 4], s[i + 5]);
+    d = fmax3(d, s[i + 6], s[i + 7]);
+  }
+  a = fmax3(a, s[124], s[125]);
+  b = fmax3(b, s[126], s[127]);
+  return fmax3(fmaxf(a, b), c, d);
+}
+
+// P = 2^(s * c2 - m_ref) for the 128 scores of a row, packed as bf16 pairs
+// (element 2i in the low half), returning the fp32 sum of the unrounded P.
+// With kTrackMax the raw row maximum is found in the same pass.
+template <bool kTrackMax>
+__device__ __forceinline__ float exp_row(const float *s, float c2, float m_ref, uint32_t *pk,
+                                         float *mx_out) {
+  const uint64_t scale2 = f2_pack(c2, c2);
+  const uint64_t neg_m2 = f2_pack(-m_ref, -m_ref);
+  uint64_t sum_a = f2_pack(0.f, 0.f), sum_b = sum_a;
+  float ma = -INFINITY, mb = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < 64; c += 2) {
+    float x0, x1, x2, x3;
+    f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), scale2, neg_m2), x0, x1);
+    f2_unpack(f2_fma(f2_pack(s[2 * c + 2], s[2 * c + 3]), scale2, neg_m2), x2, x3);
+    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+    const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+    sum_a = f2_add(sum_a, f2_pack(p0, p1));
+    sum_b = f2_add(sum_b, f2_pack(p2, p3));
+    if (kTrackMax) {
+      ma = fmax3(ma, s[2 * c], s[2 * c + 1]);
+      mb = fmax3(mb, s[2 * c + 2], s[2 * c + 3]);
+    }
+    __nv_bfloat162 h0 = __floats2bfloat162_rn(p0, p1);
+    __nv_bfloat162 h1 = __floats2bfloat162_rn(p2, p3);
+    pk[c] = *reinterpret_cast<uint32_t *>(&h0);
+    pk[c + 1] = *reinterpret_cast<uint32_t *>(&h1);
+  }
+  if (kTrackMax) *mx_out = fmaxf(ma, mb);
+  float a0, a1, b0, b1;
+  f2_unpack(sum_a, a0, a1);
+  f2_unpack(sum_b, b0, b1);
+  return (a0 + a1) + (b0 + b1);
+}
+
+
+// Softmax and epilogue for one query row (one thread; a warp covers 32 rows
+// of a 128-row tile, TMEM lane = tile row).
+//   s_addr / o_addr   TMEM address of this row's S (later P) and O columns
+//   n                 KV tiles this tile visits; bar_sfull / bar_ofull are the
+//                     mbarriers the MMA issuer commits when S(j) / the final O
+//                     are ready; signal_p() tells it P(j) is in TMEM (called by
+//                     every thread after its tcgen05 stores are fenced).
+template <int D, bool kF32Out, typename SignalP>
+__device__ __forceinline__ void softmax_row(const AttnParams &p, int row, int tile_first_row, int n,
+                                            uint32_t s_addr, uint32_t o_addr, uint32_t bar_sfull,
+                                            uint32_t bar_ofull, size_t row_index,
+                                            volatile int *abort_flag, int *err,
+                                            SignalP signal_p) {
+    const long long qpos = p.q_off + row;
+    const long long tile_first_q = p.q_off + tile_first_row;
+    const float c2 = p.scale_log2;
+    float m = -INFINITY;  // running max of scale*log2(e)*s (the reference for P)
+    float l = 0.f;        // running sum of P relative to m
+    float m_grow = -INFINITY;  // candidate new reference from the latest tile
+    bool ok = true;
+
+    for (int j = 0; j < n; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_sfull, j & 1, abort_flag, err));
+      if (!ok) break;
+      tc_fence_after();
+      const int kv0 = j * kRowsPerTile;
+      const bool tail = kv0 + kRowsPerTile > p.Skv;
+      const bool diag = p.causal && (p.kv_off + kv0 + kRowsPerTile - 1 > tile_first_q);
+      int last = 127;  // last visible column of this row in the tile
+      if (tail || diag) {
+        long long lim = static_cast<long long>(p.Skv) - kv0 - 1;
+        if (p.causal) {
+          const long long c_lim = qpos - p.kv_off - kv0;
+          lim = c_lim < lim ? c_lim : lim;
+        }
+        last = static_cast<int>(lim < -1 ? -1 : (lim > 127 ? 127 : lim));
+      }
+      // The row of S for this tile, masked (TMEM keeps S until P is written).
+      auto load_scores = [&](uint32_t (&sr)[128]) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          tmem_ld32(s_addr + 32 * i, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * i]));
+        tmem_ld_wait(sr);
+        if (tail || diag) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c > last) sr[c] = __float_as_uint(-INFINITY);
+        }
+      };
+      uint32_t pk[64];
+      float rowsum;
+      {
+        uint32_t sr[128];
+        load_scores(sr);
+        const float *s = reinterpret_cast<const float *>(sr);
+        if (j == 0) {
+          // no reference yet: the tile maximum first, then the exponentials
+          m = row_max(s) * c2;
+          rowsum = exp_row<false>(s, c2, (m == -INFINITY) ? 0.f : m, pk, nullptr);
+        } else {
+          // Exponentiate against the current reference while finding the tile
+          // maximum; only if some row's maximum grew by more than 2^8 (rare
+          // after the first tiles) is O rescaled and the pass redone.
+          float mx;
+          rowsum = exp_row<true>(s, c2, (m == -INFINITY) ? 0.f : m, pk, &mx);
+          m_grow = fmaxf(m, mx * c2);
+        }
+      }
+      if (j > 0) {
+        const float m_new = m_grow;
+        const bool grow = (m_new - m) > kRescaleThreshold;  // false while both are -inf
+        if (__any_sync(0xffffffffu, grow)) {
+          const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m - m_new);
+          m = m_new;
+          l *= alpha;
+          // O_t holds the sum through KV tile j-1: the MMA that produced it
+          // completed before S_t for tile j was signalled.
+#pragma unroll 1
+          for (int cb = 0; cb < D / 32; ++cb) {
+            uint32_t orr[32];
+            tmem_ld32(o_addr + 32 * cb, orr);
+            tmem_ld_wait(orr);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+            tmem_st32(o_addr + 32 * cb, orr);
+          }
+          tmem_st_wait();
+          uint32_t sr[128];
+          load_scores(sr);
+          rowsum = exp_row<false>(reinterpret_cast<const float *>(sr), c2,
+                                  (m == -INFINITY) ? 0.f : m, pk, nullptr);
+        }
+      }
+      l += rowsum;
+      tmem_st32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_st32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      tmem_st_wait();
+      tc_fence_before();
+      signal_p();
+    }
+
+    // ------------------------------------------------------------ epilogue
+    bool have_o = false;
+    if (ok && n > 0) {
+      have_o = __all_sync(0xffffffffu, mbar_wait(bar_ofull, 0, abort_flag, err));
+      tc_fence_after();
+    }
+    const bool row_valid = row < p.Sq;
+    const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll 1
+    for (int cb = 0; cb < D / 32; ++cb) {
+      uint32_t orr[32];
+      if (have_o) {
+        tmem_ld32(o_addr + 32 * cb, orr);
+        tmem_ld_wait(orr);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) orr[i] = 0u;
+      }
+      if (!row_valid) continue;
+      if constexpr (kF32Out) {
+        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.o) + row_index * D + cb * 32);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          dst[i] = make_float4(__uint_as_float(orr[4 * i]) * inv_l,
+                               __uint_as_float(orr[4 * i + 1]) * inv_l,
+                               __uint_as_float(orr[4 * i + 2]) * inv_l,
+                               __uint_as_float(orr[4 * i + 3]) * inv_l);
+      } else {
+        uint32_t packed[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(orr[2 * i]) * inv_l,
+                                                   __uint_as_float(orr[2 * i + 1]) * inv_l);
+          packed[i] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.o) + row_index * D +
+                                               cb * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+      }
+    }
+    if (row_valid) p.lse[row_index] = (l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
+}
+
+}  // namespace detail
+}  // namespace seqattn

@@ -18,10 +18,16 @@ struct AttnParams {
   int n_qblocks;      // ceil(Sq / 256): two 128-row query tiles per CTA
 };
 
-// Tensor maps are 3-D views [heads][rows][D] of bf16 data, box 64 x 128 x 1,
-// 128-byte swizzle; built by the caller.
-cudaError_t launch_attention(int D, bool f32_out, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                             const CUtensorMap &tm_v, const AttnParams &p, cudaStream_t stream);
+// Whether attention with head dim D runs on SM pairs (2-SM MMAs). The pair
+// kernel wants the K tensor map with 64-row boxes; every other map (and every
+// map of the single-SM kernel) uses 128-row boxes.
+bool attention_uses_pair(int D);
+
+// Tensor maps are 3-D views [heads][rows][D] of bf16 data, box 64 columns x
+// rows x 1, 128-byte swizzle; built by the caller.
+cudaError_t launch_attention(int D, bool f32_out, bool pair, const CUtensorMap &tm_q,
+                             const CUtensorMap &tm_k, const CUtensorMap &tm_v, const AttnParams &p,
+                             cudaStream_t stream);
 
 cudaError_t launch_lse_merge(const float *o_parts, const float *lse_parts, int P, long long nrows,
                              int D, void *o, bool bf16_out, float *lse, cudaStream_t stream);

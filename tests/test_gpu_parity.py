@@ -201,3 +201,39 @@ def test_full_size_workload_sampled_rows(sa, name):
     check_lse(gather_rows(lse, rows), lse_ref)
     del o, lse, qd, kd, vd
     torch.cuda.empty_cache()
+
+
+ALT_KERNEL_SCRIPT = r"""
+import sys
+sys.path.insert(0, sys.argv[1])
+import oracle, workloads
+import sequence_attn_fwd_gb300 as sa
+from tests.parity import check_o, check_lse
+for B, Hq, Hkv, S, causal in [(1, 4, 2, 700, True), (2, 2, 2, 384, False)]:
+    w = workloads.Workload("adhoc", B, Hq, Hkv, S, 128, causal, 1, 4242)
+    q, k, v = workloads.make_qkv(w)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal)
+    o, lse = sa.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal)
+    check_o(o, o_ref); check_lse(lse, lse_ref)
+    o_ref, lse_ref = oracle.attention(q, k[:, :, 128:512].contiguous(), v[:, :, 128:512].contiguous(), causal, kv_off=128)
+    o, lse = sa.attn_partial(q.cuda(), k.cuda()[:, :, 128:512], v.cuda()[:, :, 128:512], 0, 128, causal)
+    check_o(o, o_ref, bf16_out=False); check_lse(lse, lse_ref)
+sa.query_device_error()
+print("alternate kernel ok")
+"""
+
+
+def test_sm_pair_kernel_for_head_dim_128(cuda_dev):
+    """Head dim 128 runs on the single-SM kernel by default; the SM-pair kernel
+    (2-SM tcgen05 MMAs) stays selectable (SEQATTN_ATTN_KERNEL=2sm, read once per
+    process) and must stay correct."""
+    import os
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, SEQATTN_ATTN_KERNEL="2sm")
+    r = subprocess.run([sys.executable, "-c", ALT_KERNEL_SCRIPT, root], env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "alternate kernel ok" in r.stdout

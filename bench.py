@@ -185,7 +185,7 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int):
             ev[0].record(stream)
         for j in range(P):
             sa.attn_partial(qq, kk[:, :, j * C:(j + 1) * C], vv[:, :, j * C:(j + 1) * C], 0, j * C, w.causal,
-                            out=o_parts[j], lse=lse_parts[j])
+                            out=o_parts[j], lse=lse_parts[j], skip_empty=True)
         if ev:
             ev[1].record(stream)
         sa.lse_merge(o_parts, lse_parts, torch.bfloat16, out=o, lse=lse)

@@ -81,10 +81,15 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
  *   o_part    fp32 [B, Hq, Sq, D] (output, normalised by the chunk's softmax
  *             sum; rows that see no key of the chunk are 0).
  *   lse_part  fp32 [B, Hq, Sq] (output; -inf where the row sees no key).
+ *   flags     0, or ATTN_PARTIAL_SKIP_EMPTY: rows that see no key of the chunk
+ *             get lse_part = -inf and their o_part row is left unwritten (its
+ *             previous contents stay). lse_merge never reads such rows, so a
+ *             ring loop feeding lse_merge can skip those writes.
  */
+#define ATTN_PARTIAL_SKIP_EMPTY 1
 int attn_partial(const void *q, const void *k_chunk, const void *v_chunk, long long q_off,
                  long long kv_off, long long kv_head_stride, float *o_part, float *lse_part,
-                 int B, int Hq, int Hkv, int Sq, int Skv, int D, int causal, float scale,
+                 int B, int Hq, int Hkv, int Sq, int Skv, int D, int causal, float scale, int flags,
                  attn_stream_t stream);
 
 /*

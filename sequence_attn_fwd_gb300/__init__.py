@@ -25,6 +25,7 @@ __all__ = ["attn_fwd", "attn_partial", "lse_merge", "ring_attn_fwd", "ring_attn_
 RING_SCRATCH_BYTES = 64 << 20  # the library's fixed scratch array for ring_attn_fwd_static
 
 ATTN_BF16, ATTN_F32 = 0, 1
+ATTN_PARTIAL_SKIP_EMPTY = 1
 
 
 def _stream_handle(device: torch.device) -> int:
@@ -77,12 +78,15 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
 
 def attn_partial(q: torch.Tensor, k_chunk: torch.Tensor, v_chunk: torch.Tensor, q_off: int = 0,
                  kv_off: int = 0, causal: bool = False, scale: float | None = None,
-                 out: torch.Tensor | None = None, lse: torch.Tensor | None = None):
+                 out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                 skip_empty: bool = False):
     """Attention of Q [B,Hq,Sq,D] against one K/V chunk [B,Hkv,Skv,D].
 
     The chunk may be a slice along S of a larger contiguous K/V (no copy).
     q_off / kv_off are the global positions of query row 0 and key 0.
-    Returns (O_i fp32 [B,Hq,Sq,D] normalised within the chunk, lse_i fp32 [B,Hq,Sq])."""
+    Returns (O_i fp32 [B,Hq,Sq,D] normalised within the chunk, lse_i fp32 [B,Hq,Sq]).
+    Rows that see no key get lse = -inf and O = 0, or, with skip_empty, an O row
+    left unwritten (lse_merge never reads it)."""
     _require(q.dim() == 4 and k_chunk.dim() == 4 and v_chunk.shape == k_chunk.shape,
              "expected [B,H,S,D] tensors")
     B, Hq, Sq, D = q.shape
@@ -103,7 +107,8 @@ def attn_partial(q: torch.Tensor, k_chunk: torch.Tensor, v_chunk: torch.Tensor, 
     _require(lse.shape == (B, Hq, Sq) and lse.dtype == torch.float32 and lse.is_contiguous(), "bad lse")
     st = lib.attn_partial(q.data_ptr(), k_chunk.data_ptr(), v_chunk.data_ptr(), int(q_off), int(kv_off),
                           int(head_stride), out.data_ptr(), lse.data_ptr(), B, Hq, Hkv, Sq, Skv, D,
-                          int(bool(causal)), scale, _stream_handle(q.device))
+                          int(bool(causal)), scale, ATTN_PARTIAL_SKIP_EMPTY if skip_empty else 0,
+                          _stream_handle(q.device))
     _check(st, "attn_partial")
     return out, lse
 
@@ -135,7 +140,8 @@ def ring_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, cau
                   lse: torch.Tensor | None = None):
     """Ring-Attention's per-device arithmetic on one GPU: the keys are split into
     P equal chunks (S % P == 0); chunk j is attended by attn_partial at kv_off =
-    j*S/P (a zero-copy view), then the P partials are merged by lse_merge.
+    j*S/P (a zero-copy view), then the P partials are merged by lse_merge. Rows a
+    chunk cannot see are not written in o_parts (their lse is -inf).
     o_parts / lse_parts are optional preallocated fp32 [P,B,Hq,S,D] / [P,B,Hq,S]."""
     B, Hq, S, D = q.shape
     _require(P >= 1 and S % P == 0, "S must be a multiple of P")
@@ -146,7 +152,7 @@ def ring_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, cau
         lse_parts = torch.empty((P, B, Hq, S), dtype=torch.float32, device=q.device)
     for j in range(P):
         attn_partial(q, k[:, :, j * C:(j + 1) * C], v[:, :, j * C:(j + 1) * C], 0, j * C, causal, scale,
-                     out=o_parts[j], lse=lse_parts[j])
+                     out=o_parts[j], lse=lse_parts[j], skip_empty=True)
     return lse_merge(o_parts, lse_parts, torch.bfloat16, out=out, lse=lse)
 
 

@@ -34,7 +34,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L = ctypes.CDLL(path)
     P, I, LL, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_float
     L.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P]
-    L.attn_partial.argtypes = [P, P, P, LL, LL, LL, P, P, I, I, I, I, I, I, I, F, P]
+    L.attn_partial.argtypes = [P, P, P, LL, LL, LL, P, P, I, I, I, I, I, I, I, F, I, P]
     L.lse_merge.argtypes = [P, P, I, P, I, P, I, I, I, I, P]
     L.attn_query_device_error.argtypes = [P]
     L.attn_status_string.argtypes = [I]

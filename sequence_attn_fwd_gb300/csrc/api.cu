@@ -66,7 +66,8 @@ constexpr long long kMaxRowsPerHead = 1ll << 30;  // keeps every row index withi
 
 int run_attention(const void *q, const void *k, const void *v, long long q_off, long long kv_off,
                   long long kv_head_stride, void *o, float *lse, int B, int Hq, int Hkv, int Sq,
-                  int Skv, int D, int causal, float scale, bool f32_out, cudaStream_t stream) {
+                  int Skv, int D, int causal, float scale, bool f32_out, bool skip_empty,
+                  cudaStream_t stream) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Skv < 0) return ATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
@@ -107,6 +108,7 @@ int run_attention(const void *q, const void *k, const void *v, long long q_off, 
   p.scale_log2 = scale * 1.4426950408889634f;
   p.causal = causal;
   p.n_qblocks = (Sq + 255) / 256;
+  p.skip_empty = skip_empty ? 1 : 0;
   cudaError_t e = seqattn::launch_attention(D, f32_out, pair, tq, tk, tv, p, stream);
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
@@ -117,16 +119,18 @@ extern "C" {
 
 int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
              int Hkv, int S, int D, int causal, float scale, attn_stream_t stream) {
-  return run_attention(q, k, v, 0, 0, 0, o, lse, B, Hq, Hkv, S, S, D, causal, scale, false,
+  return run_attention(q, k, v, 0, 0, 0, o, lse, B, Hq, Hkv, S, S, D, causal, scale, false, false,
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
 int attn_partial(const void *q, const void *k_chunk, const void *v_chunk, long long q_off,
                  long long kv_off, long long kv_head_stride, float *o_part, float *lse_part,
-                 int B, int Hq, int Hkv, int Sq, int Skv, int D, int causal, float scale,
+                 int B, int Hq, int Hkv, int Sq, int Skv, int D, int causal, float scale, int flags,
                  attn_stream_t stream) {
+  if (flags & ~ATTN_PARTIAL_SKIP_EMPTY) return ATTN_ERR_INVALID_ARG;
   return run_attention(q, k_chunk, v_chunk, q_off, kv_off, kv_head_stride, o_part, lse_part, B, Hq,
-                       Hkv, Sq, Skv, D, causal, scale, true, reinterpret_cast<cudaStream_t>(stream));
+                       Hkv, Sq, Skv, D, causal, scale, true, (flags & ATTN_PARTIAL_SKIP_EMPTY) != 0,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 int lse_merge(const float *o_parts, const float *lse_parts, int P, void *o, int o_dtype,
@@ -231,8 +235,9 @@ extern "C" int attn_ring_fwd_static(const void *q, const void *k, const void *v,
   float *o_parts = static_cast<float *>(scratch);
   float *lse_parts = reinterpret_cast<float *>(static_cast<unsigned char *>(scratch) + o_bytes);
   // Every partial element the merge reads is written by the hops of this same
-  // call (rows a chunk cannot see get O = 0, lse = -inf), so nothing left in
-  // the array by an earlier call needs clearing.
+  // call: each hop writes every lse, and the O rows of every row with a finite
+  // lse (rows a chunk cannot see get lse = -inf and are never read), so
+  // nothing left in the array by an earlier call needs clearing.
   const int C = S / P;
   for (int j = 0; j < P; ++j) {
     const size_t kv_offset = static_cast<size_t>(j) * C * D;  // elements: chunk j of every head
@@ -240,7 +245,7 @@ extern "C" int attn_ring_fwd_static(const void *q, const void *k, const void *v,
                       static_cast<const unsigned char *>(v) + kv_offset * 2, 0,
                       static_cast<long long>(j) * C, static_cast<long long>(S) * D,
                       o_parts + static_cast<size_t>(j) * rows * D, lse_parts + static_cast<size_t>(j) * rows,
-                      B, Hq, Hkv, S, C, D, causal, scale, stream);
+                      B, Hq, Hkv, S, C, D, causal, scale, ATTN_PARTIAL_SKIP_EMPTY, stream);
     if (st != ATTN_OK) return st;
   }
   return lse_merge(o_parts, lse_parts, P, o, ATTN_BF16, lse, B, Hq, S, D, stream);

@@ -85,6 +85,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int row0 = qb * kRowsPerCluster;
   int *err = &g_device_error;
 
+  // No row of the cluster's 512 sees a key: both CTAs reach the same decision
+  // and leave before any cluster-wide operation.
+  {
+    bool any = false;
+    for (int r = 0; r < kRowsPerCluster; r += kRowsPerTile) any = any || kv_tiles_for(p, row0 + r) > 0;
+    if (!any) {
+      for (int g = 0; g < 2; ++g)
+        write_empty_rows<kD, kF32Out>(p, bh, row0 + 256 * g + kRowsPerTile * static_cast<int>(rank),
+                                      kRowsPerTile);
+      return;
+    }
+  }
+
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQ), 1);
     mbar_init(bar(kBarQPeer), 1);

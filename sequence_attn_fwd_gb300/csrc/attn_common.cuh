@@ -80,6 +80,22 @@ __device__ __forceinline__ float exp_row(const float *s, float c2, float m_ref, 
 }
 
 
+// A block of query rows none of which sees a key: lse = -inf and, unless the
+// caller asked to skip them, O = 0. The rows of one head are contiguous in
+// memory, so the zero fill is one coalesced run of 16-byte stores by the CTA.
+template <int D, bool kF32Out>
+__device__ __forceinline__ void write_empty_rows(const AttnParams &p, int bh, int row_begin,
+                                                 int nrows) {
+  const int rows = min(nrows, p.Sq - row_begin);
+  if (rows <= 0) return;
+  const size_t base = static_cast<size_t>(bh) * p.Sq + row_begin;
+  for (int i = threadIdx.x; i < rows; i += blockDim.x) p.lse[base + i] = -INFINITY;
+  if (p.skip_empty) return;
+  const size_t n16 = static_cast<size_t>(rows) * D * (kF32Out ? 4 : 2) / 16;
+  uint4 *dst = reinterpret_cast<uint4 *>(static_cast<char *>(p.o) + base * D * (kF32Out ? 4 : 2));
+  for (size_t i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 // Softmax and epilogue for one query row (one thread; a warp covers 32 rows
 // of a 128-row tile, TMEM lane = tile row).
 //   s_addr / o_addr   TMEM address of this row's S (later P) and O columns
@@ -189,6 +205,7 @@ __device__ __forceinline__ void softmax_row(const AttnParams &p, int row, int ti
       tc_fence_after();
     }
     const bool row_valid = row < p.Sq;
+    const bool write_o = row_valid && !(p.skip_empty && l == 0.f);
     const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll 1
     for (int cb = 0; cb < D / 32; ++cb) {
@@ -200,7 +217,7 @@ __device__ __forceinline__ void softmax_row(const AttnParams &p, int row, int ti
 #pragma unroll
         for (int i = 0; i < 32; ++i) orr[i] = 0u;
       }
-      if (!row_valid) continue;
+      if (!write_o) continue;
       if constexpr (kF32Out) {
         float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.o) + row_index * D + cb * 32);
 #pragma unroll

@@ -90,6 +90,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int row0 = qblock * 2 * kRowsPerTile;
   int *err = &g_device_error;
 
+  // No row of this block sees a key (rows past the end, or a causal chunk that
+  // lies entirely after them): no pipeline needed.
+  if (kv_tiles_for(p, row0) == 0 && kv_tiles_for(p, row0 + kRowsPerTile) == 0) {
+    write_empty_rows<D, kF32Out>(p, bh, row0, 2 * kRowsPerTile);
+    return;
+  }
+
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQ), 1);
     for (int s = 0; s < C::kStages; ++s) {

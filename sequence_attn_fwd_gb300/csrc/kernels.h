@@ -16,6 +16,7 @@ struct AttnParams {
   float scale_log2;   // softmax scale times log2(e)
   int causal;
   int n_qblocks;      // ceil(Sq / 256): two 128-row query tiles per CTA
+  int skip_empty;     // rows that see no key: write lse = -inf only, leave O untouched
 };
 
 // Whether attention with head dim D runs on SM pairs (2-SM MMAs). The pair

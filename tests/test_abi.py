@@ -76,15 +76,17 @@ def test_attn_fwd_argument_checks(lib):
 
 
 def test_attn_partial_argument_checks(lib):
-    def part(kv_head_stride=0, Sq=16, Skv=16, D=64, o=FAKE):
+    def part(kv_head_stride=0, Sq=16, Skv=16, D=64, o=FAKE, flags=0):
         return lib.attn_partial(FAKE, FAKE, FAKE, 0, 0, kv_head_stride, o, FAKE, 1, 2, 1, Sq, Skv, D, 1,
-                                ctypes.c_float(0.125), None)
+                                ctypes.c_float(0.125), flags, None)
 
     assert part(kv_head_stride=16 * 64 - 8) == 1  # stride shorter than a head
     assert part(kv_head_stride=16 * 64 + 4) == 1  # not a multiple of 8 elements
     assert part(o=FAKE + 4) == 1
     assert part(D=32) == 2
     assert part(Sq=0) == 0
+    assert part(flags=2) == 1 and part(flags=-1) == 1  # unknown flag bits
+    assert part(Sq=0, flags=1) == 0
 
 
 def test_lse_merge_argument_checks(lib):

@@ -131,6 +131,26 @@ def test_attn_partial_chunk_invisible_to_every_row(sa):
     assert (o == 0).all() and torch.isneginf(lse).all()
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_attn_partial_skip_empty_leaves_invisible_rows_untouched(sa, D):
+    """Chunk [600, 900) of 1000 keys under causal masking: query rows < 600 see none
+    of it (whole 256-row blocks and part of one tile). With skip_empty their O rows
+    keep their previous contents and their lse is -inf; all other rows match."""
+    B, Hq, Hkv, S = 1, 4, 2, 1000
+    a, b = 600, 900
+    q, k, v = workloads.make_qkv(adhoc(B, Hq, Hkv, S, D, True, seed=13))
+    o_ref, lse_ref = oracle.attention(q, k[:, :, a:b].contiguous(), v[:, :, a:b].contiguous(), True, kv_off=a)
+    qd, kd, vd = to_dev(q, k, v)
+    out = torch.full((B, Hq, S, D), 7.0, dtype=torch.float32, device="cuda")
+    o, lse = sa.attn_partial(qd, kd[:, :, a:b], vd[:, :, a:b], 0, a, True, out=out, skip_empty=True)
+    torch.cuda.synchronize()
+    check_lse(lse, lse_ref)
+    empty = torch.isneginf(lse)
+    assert empty[:, :, :a].all() and not empty[:, :, a:].any()
+    assert (o[:, :, :a] == 7.0).all()
+    check_o(o[:, :, a:], o_ref[:, :, a:], bf16_out=False)
+
+
 def test_ring_reduced_size_against_oracle_and_single_pass(sa):
     w = W["ring8_b2h32s4096d128_causal"]
     S = 1024

@@ -121,6 +121,17 @@ const char *attn_status_string(int status);
 /* The cudaError_t of the most recent ATTN_ERR_CUDA (0 if none). */
 int attn_last_cuda_error(void);
 
+/*
+ * attn_debug_expire_wait -- test hook for the bounded-wait path (no
+ * counterpart on the pages). Enqueues a one-CTA kernel that waits on an
+ * mbarrier nothing ever arrives at; after timeout_us (1 .. 1e6) the wait gives
+ * up the same way a stuck attention pipeline's wait does: it records a
+ * timeout in the device error word. Until attn_query_device_error() reports
+ * and clears it, later attention launches skip their work (every row comes
+ * out as O = 0, lse = -inf). Faults nothing; the context stays usable.
+ */
+int attn_debug_expire_wait(unsigned timeout_us, attn_stream_t stream);
+
 /* Size of the library's fixed scratch array used by attn_ring_fwd_static. */
 #define SEQATTN_RING_SCRATCH_BYTES (64ull << 20) /* 64 MiB */
 

@@ -286,6 +286,26 @@ cudaError_t launch_attention(int D, bool f32_out, bool pair, const CUtensorMap &
                  : launch_typed<64, false>(tq, tk, tv, p, stream);
 }
 
+// A one-CTA kernel waiting on an mbarrier that nothing ever arrives at, with
+// a short limit: the wait gives up exactly as a stuck attention pipeline's
+// would, recording the timeout in the device error word.
+__global__ void expire_wait_kernel(unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(smem_addr(&bar), 0, &abort_flag, &g_device_error, limit_ns);
+}
+
+cudaError_t launch_expire_wait(unsigned timeout_us, cudaStream_t stream) {
+  expire_wait_kernel<<<1, 32, 0, stream>>>(static_cast<unsigned long long>(timeout_us) * 1000ull);
+  return cudaGetLastError();
+}
+
 cudaError_t read_and_clear_device_error(int *code) {
   int zero = 0;
   cudaError_t e = cudaMemcpyFromSymbol(code, g_device_error, sizeof(int));

@@ -33,6 +33,9 @@ cudaError_t launch_attention(int D, bool f32_out, bool pair, const CUtensorMap &
 cudaError_t launch_lse_merge(const float *o_parts, const float *lse_parts, int P, long long nrows,
                              int D, void *o, bool bf16_out, float *lse, cudaStream_t stream);
 
+// One CTA waits on an mbarrier nothing arrives at until timeout_us runs out.
+cudaError_t launch_expire_wait(unsigned timeout_us, cudaStream_t stream);
+
 // Reads and clears the device error word (after the caller synchronised).
 cudaError_t read_and_clear_device_error(int *code);
 

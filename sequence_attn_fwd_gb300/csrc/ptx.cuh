@@ -57,7 +57,8 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 // recorded an error in the device error word, or if the wait ran out of
 // time, in which case it sets the flag and the device error word.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          int *err_word) {
+                                          int *err_word,
+                                          uint64_t limit_ns = SEQATTN_WAIT_TIMEOUT_NS) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t n = 1;; ++n) {
@@ -68,7 +69,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         *abort_flag = 1;
         return false;
       }
-      if (global_timer_ns() - t0 > SEQATTN_WAIT_TIMEOUT_NS) {
+      if (global_timer_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         atomicExch(err_word, kErrTimeout);
         return false;

@@ -31,7 +31,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted(["attn_fwd", "attn_partial", "lse_merge", "attn_query_device_error",
                                            "attn_status_string", "attn_last_cuda_error",
-                                           "attn_ring_fwd_static"])
+                                           "attn_ring_fwd_static", "attn_debug_expire_wait"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -46,6 +46,11 @@ def test_library_is_built_for_sm103a():
     log = open(os.path.join(os.path.dirname(build_mod.LIB), "ptxas.log")).read()
     assert "for 'sm_103a'" in log and "attn_fwd_kernel" in log and "lse_merge_kernel" in log
     assert "tcgen05" in open(os.path.join(build_mod.CSRC, "ptx.cuh")).read()
+
+
+def test_expire_wait_argument_checks(lib):
+    assert lib.attn_debug_expire_wait(0, None) == 1
+    assert lib.attn_debug_expire_wait(2_000_000, None) == 1
 
 
 def test_status_strings(lib):

@@ -90,6 +90,42 @@ def merge_algorithmic_bytes(w: workloads.Workload, out_bytes: int = 2) -> int:
     return w.P * rows * 4 + finite_rows * w.D * 4 + rows * w.D * out_bytes + rows * 4
 
 
+KERNEL_SOURCES = {
+    "attn_partial": ["attn_kernel.cu", "attn_common.cuh", "ptx.cuh"],
+    "attn_fwd": ["attn_kernel.cu", "attn_common.cuh", "ptx.cuh"],
+    "lse_merge": ["lse_merge.cu"],
+}
+
+
+def sources_digest(kernel: str) -> str:
+    """SHA-256 prefix of the sources a kernel is built from."""
+    import hashlib
+
+    m = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "sequence_attn_fwd_gb300", "csrc", f), "rb") as fh:
+            m.update(fh.read())
+    return m.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str, profiles_dir: str = os.path.join(ROOT, "profiles")):
+    """DRAM bytes per launch from a committed ncu summary (a line
+    `traffic <kernel> <workload> bytes_per_launch=<n> sources=<digest>`), or None
+    when there is none or the kernel's sources changed since it was captured."""
+    import glob
+    import re
+
+    digest = sources_digest(kernel)
+    pat = re.compile(r"^traffic (\S+) (\S+) bytes_per_launch=(\d+) sources=([0-9a-f]+)\s*$")
+    for path in sorted(glob.glob(os.path.join(profiles_dir, "*.md"))):
+        with open(path) as f:
+            for line in f:
+                m = pat.match(line.strip())
+                if m and m.group(1) == kernel and m.group(2) == workload and m.group(4) == digest:
+                    return int(m.group(3))
+    return None
+
+
 def max_over_ranks(value: float) -> float:
     import torch.distributed as dist
 
@@ -263,7 +299,8 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int):
     flops_per_launch = F / (P if P > 1 else 1)
     achieved = flops_per_launch / (attn_avg_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                "frac": achieved / peaks["bf16_tflops"],
+                "traffic": measured_traffic("attn_partial" if P > 1 else "attn_fwd", w.name),
                 "kernel": ("attn_fwd_2sm_kernel" if D == 128 and os.environ.get("SEQATTN_ATTN_KERNEL") == "2sm"
                            else f"attn_fwd_kernel<{D}>") + ("<f32 out> (attn_partial)" if P > 1 else "<bf16 out>"),
                 "peak_source": f"{peak_src} bf16 burst", "launch_ms": attn_avg_ms}
@@ -273,7 +310,8 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int):
         mms = statistics.mean(merge_ms)
         gbs = mb / (mms * 1e-3) / 1e9
         merge = {"achieved": gbs, "unit": "GB/s", "peak": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"],
-                 "launch_ms": mms, "algorithmic_bytes": mb, "peak_source": f"{peak_src} copy"}
+                 "launch_ms": mms, "algorithmic_bytes": mb, "peak_source": f"{peak_src} copy",
+                 "traffic": measured_traffic("lse_merge", w.name)}
     return {
         "value": value, "ms_per_step": ms_per_step, "e2e": e2e, "roofline": roofline, "merge": merge,
         "gpu_launches": args.steps * launches_per_step, "clocks": clocks,

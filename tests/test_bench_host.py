@@ -1,0 +1,108 @@
+"""Host logic of bench.py, on the CPU: the replica path's max-over-ranks timing
+with two gloo ranks, the algorithmic counts the roofline uses, the clock summary
+and the peak-file loader."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+import workloads
+
+
+def _rank_main(rank, world, port, values, out_dir):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        got = bench.max_over_ranks(values[rank])
+        with open(os.path.join(out_dir, f"r{rank}.json"), "w") as f:
+            json.dump(got, f)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_two_gloo_ranks(tmp_path):
+    import random
+
+    port = 29500 + random.randint(0, 2000)
+    values = [3.5, 7.25]
+    mp.start_processes(_rank_main, args=(2, port, values, str(tmp_path)), nprocs=2, join=True,
+                       start_method="spawn")
+    for r in range(2):
+        assert json.load(open(tmp_path / f"r{r}.json")) == 7.25
+
+
+def test_max_over_ranks_single_process_is_identity():
+    assert bench.max_over_ranks(1.5) == 1.5
+
+
+def test_visible_pairs_matches_brute_force():
+    for S_q, q_off, kv_len, kv_off, causal in [(37, 0, 37, 0, True), (50, 10, 20, 25, True), (9, 0, 13, 0, False),
+                                               (64, 0, 16, 48, True), (16, 0, 16, 40, True)]:
+        brute = sum(1 for r in range(S_q) for j in range(kv_len)
+                    if not causal or kv_off + j <= q_off + r)
+        assert bench.visible_pairs(S_q, q_off, kv_len, kv_off, causal) == brute
+
+
+def test_causal_flops_count_equals_chunked_visible_pairs():
+    """F = 4 B Hq S^2 D / 2 is the convention; the exact visible pairs add the diagonal."""
+    w = workloads.WORKLOADS["ring8_b2h32s4096d128_causal"]
+    pairs = sum(bench.visible_pairs(w.S, 0, w.chunk, j * w.chunk, True) for j in range(w.P))
+    assert pairs == w.S * (w.S + 1) // 2
+    assert math.isclose(w.attention_flops(), 4.0 * w.B * w.Hq * w.D * w.S * w.S / 2)
+
+
+def test_merge_algorithmic_bytes_ring8():
+    w = workloads.WORKLOADS["ring8_b2h32s4096d128_causal"]
+    rows = w.B * w.Hq * w.S
+    finite_rows = sum(w.B * w.Hq * (w.S - c * w.chunk) for c in range(w.P))
+    assert finite_rows * 64 == w.P * rows * 36  # 36/64 of the P dense partials' rows are finite
+    expected = w.P * rows * 4 + finite_rows * w.D * 4 + rows * w.D * 2 + rows * 4
+    assert bench.merge_algorithmic_bytes(w) == expected
+    assert abs(expected - 0.6805e9) < 1e6
+
+
+def test_summarise_clocks():
+    lines = ["0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+             "0, 1980, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active",
+             "0, 2070, 2070, 1000.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+             "garbage line"]
+    s = bench.summarise_clocks(lines)
+    assert s == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+    assert bench.summarise_clocks([])["samples"] == 0
+
+
+def test_load_peaks(tmp_path):
+    peaks, src = bench.load_peaks(str(tmp_path / "missing.json"))
+    assert src == "fallback" and peaks["bf16_tflops"] == 1900.0 and peaks["hbm_gbs"] == 6800.0
+    p = tmp_path / "peaks.json"
+    p.write_text(json.dumps({"hbm_gbs": 7000.5, "bf16_tflops": {"value": 2000.0}}))
+    peaks, src = bench.load_peaks(str(p))
+    assert src == "measured" and peaks == {"hbm_gbs": 7000.5, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 2000.0}
+
+
+def test_workload_sizes_match_the_stated_configurations():
+    W = workloads.WORKLOADS
+    assert [(w.B, w.Hq, w.Hkv, w.S, w.D, w.causal, w.P) for w in W.values()] == [
+        (1, 2, 2, 256, 64, False, 1), (2, 32, 32, 4096, 128, True, 8), (1, 28, 4, 32768, 128, True, 1),
+        (2, 32, 32, 8192, 128, True, 16), (1, 32, 8, 131072, 128, True, 16)]
+    w = W["gqa_b1hq28hkv4s32768d128_causal"]
+    pos = workloads.boost_positions(w)
+    assert len(pos) == 327 and len(np.unique(pos)) == 327
+    rows = workloads.sample_query_rows(W["ring16_b1hq32hkv8s131072d128_causal"])
+    assert rows.shape == (32, 64) and all(len(np.unique(r)) == 64 for r in rows)
+
+
+def test_measured_traffic_follows_the_kernel_sources(tmp_path):
+    digest = bench.sources_digest("lse_merge")
+    (tmp_path / "x.md").write_text(
+        "text\n```\ntraffic lse_merge wl bytes_per_launch=123 sources=%s\n"
+        "traffic lse_merge other bytes_per_launch=9 sources=0000000000000000\n```\n" % digest)
+    assert bench.measured_traffic("lse_merge", "wl", str(tmp_path)) == 123
+    assert bench.measured_traffic("lse_merge", "other", str(tmp_path)) is None  # stale capture
+    assert bench.measured_traffic("attn_partial", "wl", str(tmp_path)) is None

@@ -60,6 +60,24 @@ bool make_map(CUtensorMap *map, const void *base, int D, long long rows, long lo
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D view [heads][rows][D] of the output (fp32 or bf16, rows contiguous per
+// head); box 128 bytes x 128 rows x 1 with 128-byte swizzle, for TMA stores.
+bool make_out_map(CUtensorMap *map, void *base, int D, long long rows, long long heads,
+                  bool f32) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const unsigned es = f32 ? 4u : 2u;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * es,
+                           static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(D) * es};
+  cuuint32_t box[3] = {128u / es, 128u, 1u};
+  cuuint32_t estride[3] = {1u, 1u, 1u};
+  return fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base,
+            dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool scale_ok(float scale) { return isfinite(scale) && scale > 0.f; }
 
 constexpr long long kMaxRowsPerHead = 1ll << 30;  // keeps every row index within int range
@@ -85,14 +103,15 @@ int run_attention(const void *q, const void *k, const void *v, long long q_off, 
       (reinterpret_cast<uintptr_t>(lse) & 3u))
     return ATTN_ERR_INVALID_ARG;
 
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   const bool pair = seqattn::attention_uses_pair(D);
   // An empty key set still needs well-formed maps; no KV tile is ever loaded.
   const long long kv_rows = Skv > 0 ? Skv : 1;
   if (!make_map(&tq, q, D, Sq, static_cast<long long>(B) * Hq, static_cast<long long>(Sq) * D) ||
       !make_map(&tk, k, D, kv_rows, static_cast<long long>(B) * Hkv, kv_head_stride,
                 pair ? 64u : 128u) ||
-      !make_map(&tv, v, D, kv_rows, static_cast<long long>(B) * Hkv, kv_head_stride))
+      !make_map(&tv, v, D, kv_rows, static_cast<long long>(B) * Hkv, kv_head_stride) ||
+      !make_out_map(&to, o, D, Sq, static_cast<long long>(B) * Hq, f32_out))
     return cuda_fail(cudaErrorInvalidValue);
 
   seqattn::AttnParams p;
@@ -109,7 +128,7 @@ int run_attention(const void *q, const void *k, const void *v, long long q_off, 
   p.causal = causal;
   p.n_qblocks = (Sq + 255) / 256;
   p.skip_empty = skip_empty ? 1 : 0;
-  cudaError_t e = seqattn::launch_attention(D, f32_out, pair, tq, tk, tv, p, stream);
+  cudaError_t e = seqattn::launch_attention(D, f32_out, pair, tq, tk, tv, to, p, stream);
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 

@@ -254,7 +254,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t pfull_leader = mapa_shared(pfull_local, 0);
     softmax_row<kD, kF32Out>(p, row, tile_first, g ? n_grp[1] : n_grp[0], tS(g) + lane_off,
                              tO(g) + lane_off, bar(kBarSFull + g), bar(kBarOFull + g),
-                             static_cast<size_t>(bh) * p.Sq + row, abort_flag, err, [&] {
+                             static_cast<size_t>(bh) * p.Sq + row, abort_flag, err,
+                             EpilogueStore{nullptr, 0u, 0, 0}, [&] {
                                __syncwarp();
                                if (lane == 0) {
                                  if (leader)

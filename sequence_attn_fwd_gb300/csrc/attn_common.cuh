@@ -96,6 +96,20 @@ __device__ __forceinline__ void write_empty_rows(const AttnParams &p, int bh, in
   for (size_t i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
+// How a warpgroup's epilogue writes its 128-row O tile. With a tensor map the
+// tile leaves through shared memory: each thread puts its row's 128-byte slice
+// of a column chunk into a 128-byte-swizzled staging box (conflict-free), and
+// one thread stores the box with TMA, so global writes are whole lines instead
+// of one 16-byte piece of 32 different rows per warp store. Without a map each
+// thread stores its own row.
+struct EpilogueStore {
+  const CUtensorMap *map;  // O as [heads][rows][D], box 128 bytes x 128 rows x 1, 128-byte swizzle
+  uint32_t stage;          // shared address of D/64 staging boxes of 16 KB, 1024-byte aligned,
+                           // free once this tile's final O is signalled
+  int named_bar;           // barrier id private to the warpgroup (128 threads)
+  int head;                // third map coordinate, b * Hq + hq
+};
+
 // Softmax and epilogue for one query row (one thread; a warp covers 32 rows
 // of a 128-row tile, TMEM lane = tile row).
 //   s_addr / o_addr   TMEM address of this row's S (later P) and O columns
@@ -108,7 +122,7 @@ __device__ __forceinline__ void softmax_row(const AttnParams &p, int row, int ti
                                             uint32_t s_addr, uint32_t o_addr, uint32_t bar_sfull,
                                             uint32_t bar_ofull, size_t row_index,
                                             volatile int *abort_flag, int *err,
-                                            SignalP signal_p) {
+                                            const EpilogueStore &store, SignalP signal_p) {
     const long long qpos = p.q_off + row;
     const long long tile_first_q = p.q_off + tile_first_row;
     const float c2 = p.scale_log2;
@@ -207,6 +221,69 @@ __device__ __forceinline__ void softmax_row(const AttnParams &p, int row, int ti
     const bool row_valid = row < p.Sq;
     const bool write_o = row_valid && !(p.skip_empty && l == 0.f);
     const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+    bool via_tma = store.map != nullptr;
+    if (via_tma) {
+      // Whole-box stores need the final O on every row, no row that must stay
+      // unwritten (skip_empty rows before the chunk's first key) and a first
+      // row inside the tensor.
+      const bool keep_rows = p.skip_empty && p.causal && (p.q_off + tile_first_row < p.kv_off);
+      via_tma = named_bar_and(store.named_bar, 128, have_o) && !keep_rows && tile_first_row < p.Sq;
+    }
+    if (via_tma) {
+      constexpr int kChunkCols = kF32Out ? 32 : 64;  // 128 bytes of a row
+      constexpr int kChunks = D / kChunkCols;
+      constexpr int kBufs = D / 64;
+      const bool leader = (threadIdx.x & 127) == 0;
+      const uint32_t row_in_tile = static_cast<uint32_t>(row - tile_first_row);
+      const uint32_t swz = row_in_tile & 7u;
+#pragma unroll 1
+      for (int c = 0; c < kChunks; ++c) {
+        uint32_t v[32];
+        if constexpr (kF32Out) {
+          tmem_ld32(o_addr + 32 * c, v);
+          tmem_ld_wait(v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * inv_l);
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t orr[32];
+            tmem_ld32(o_addr + 64 * c + 32 * h, orr);
+            tmem_ld_wait(orr);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(orr[2 * i]) * inv_l,
+                                                        __uint_as_float(orr[2 * i + 1]) * inv_l);
+              v[16 * h + i] = *reinterpret_cast<uint32_t *>(&b2);
+            }
+          }
+        }
+        const uint32_t buf = store.stage + static_cast<uint32_t>(c % kBufs) * 16384u;
+        if (c >= kBufs) {
+          // the box stored from this buffer kBufs chunks ago must have been read
+          if (leader) bulk_wait_group_read<kBufs - 1>();
+          __syncwarp();
+          named_bar_sync(store.named_bar, 128);
+        }
+        const uint32_t dst = buf + row_in_tile * 128u;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          st_shared_v4(dst + ((static_cast<uint32_t>(k) ^ swz) << 4), v[4 * k], v[4 * k + 1],
+                       v[4 * k + 2], v[4 * k + 3]);
+        fence_proxy_async_shared();
+        __syncwarp();
+        named_bar_sync(store.named_bar, 128);
+        if (leader) {
+          tma_store_3d(store.map, buf, c * kChunkCols, tile_first_row, store.head);
+          bulk_commit_group();
+        }
+      }
+      // The staging boxes are shared memory of this CTA: every store must be
+      // complete before the CTA may exit.
+      if (leader) bulk_wait_all();
+      if (row_valid) p.lse[row_index] = (l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
+      return;
+    }
 #pragma unroll 1
     for (int cb = 0; cb < D / 32; ++cb) {
       uint32_t orr[32];

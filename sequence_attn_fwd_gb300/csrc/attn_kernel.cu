@@ -63,7 +63,8 @@ template <int D, bool kF32Out>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_o, const AttnParams p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -228,10 +229,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = row0 + t * kRowsPerTile + row_in_tile;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t pfull = bar(kBarPFull + t);
+    // Query tile t's shared memory is free once O_t is final: every S_t MMA
+    // was issued before the last PV_t MMA, and MMAs complete in issue order.
+    const EpilogueStore store{&tm_o, smem_addr(sQ + t * C::kTileBytes), 1 + t, bh};
     softmax_row<D, kF32Out>(p, row, row0 + t * kRowsPerTile, t ? n_tiles[1] : n_tiles[0],
                             tS(t) + lane_off, tO(t) + lane_off, bar(kBarSFull + t),
                             bar(kBarOFull + t), static_cast<size_t>(bh) * p.Sq + row, abort_flag, err,
-                            [&] {
+                            store, [&] {
                               __syncwarp();
                               if (lane == 0) mbar_arrive(pfull);  // one arrival per warp
                             });
@@ -247,13 +251,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool kF32Out>
 cudaError_t launch_typed(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                         const AttnParams &p, cudaStream_t stream) {
+                         const CUtensorMap &to, const AttnParams &p, cudaStream_t stream) {
   auto kernel = attn_fwd_kernel<D, kF32Out>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg<D>::kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(p.B * p.Hq), static_cast<unsigned>(p.n_qblocks));
-  kernel<<<grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, p);
+  kernel<<<grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
@@ -276,14 +280,14 @@ bool attention_uses_pair(int D) {
 }
 
 cudaError_t launch_attention(int D, bool f32_out, bool pair, const CUtensorMap &tq,
-                             const CUtensorMap &tk, const CUtensorMap &tv, const AttnParams &p,
-                             cudaStream_t stream) {
+                             const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &to,
+                             const AttnParams &p, cudaStream_t stream) {
   if (pair) return f32_out ? pair2sm::launch_pair<true>(tq, tk, tv, p, stream)
                            : pair2sm::launch_pair<false>(tq, tk, tv, p, stream);
-  if (D == 128) return f32_out ? launch_typed<128, true>(tq, tk, tv, p, stream)
-                               : launch_typed<128, false>(tq, tk, tv, p, stream);
-  return f32_out ? launch_typed<64, true>(tq, tk, tv, p, stream)
-                 : launch_typed<64, false>(tq, tk, tv, p, stream);
+  if (D == 128) return f32_out ? launch_typed<128, true>(tq, tk, tv, to, p, stream)
+                               : launch_typed<128, false>(tq, tk, tv, to, p, stream);
+  return f32_out ? launch_typed<64, true>(tq, tk, tv, to, p, stream)
+                 : launch_typed<64, false>(tq, tk, tv, to, p, stream);
 }
 
 // A one-CTA kernel waiting on an mbarrier that nothing ever arrives at, with

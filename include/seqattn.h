@@ -132,6 +132,16 @@ int attn_last_cuda_error(void);
  */
 int attn_debug_expire_wait(unsigned timeout_us, attn_stream_t stream);
 
+/*
+ * attn_debug_exp2 -- test hook for the softmax exponentials (no counterpart on
+ * the pages): y[i] = 2^x[i] computed by the same device code the attention
+ * kernels use, the FMA-pipe polynomial (poly = 1) or the MUFU ex2 (poly = 0).
+ * x, y: device fp32 arrays of n elements (owned by the caller). Asynchronous
+ * on `stream`. ATTN_ERR_INVALID_ARG for n < 0, a null pointer with n > 0, or
+ * poly other than 0 / 1.
+ */
+int attn_debug_exp2(const float *x, float *y, long long n, int poly, attn_stream_t stream);
+
 /* Size of the library's fixed scratch array used by attn_ring_fwd_static. */
 #define SEQATTN_RING_SCRATCH_BYTES (64ull << 20) /* 64 MiB */
 

@@ -14,7 +14,7 @@ LIB_PATH = os.path.join(_PKG, "lib", "libseqattn.so")
 # Every function the public header include/seqattn.h declares.
 EXPORTS = ["attn_fwd", "attn_partial", "lse_merge", "attn_query_device_error",
            "attn_status_string", "attn_last_cuda_error", "attn_ring_fwd_static",
-           "attn_debug_expire_wait"]
+           "attn_debug_expire_wait", "attn_debug_exp2"]
 
 STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
           3: "ATTN_ERR_CUDA", 4: "ATTN_ERR_TIMEOUT"}
@@ -45,6 +45,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.attn_ring_fwd_static.restype = ctypes.c_int
     L.attn_debug_expire_wait.argtypes = [ctypes.c_uint, P]
     L.attn_debug_expire_wait.restype = ctypes.c_int
+    L.attn_debug_exp2.argtypes = [P, P, ctypes.c_longlong, ctypes.c_int, P]
+    L.attn_debug_exp2.restype = ctypes.c_int
     for name in ("attn_fwd", "attn_partial", "lse_merge", "attn_query_device_error",
                  "attn_last_cuda_error"):
         getattr(L, name).restype = ctypes.c_int

@@ -190,6 +190,14 @@ const char *attn_status_string(int status) {
 
 int attn_last_cuda_error(void) { return g_last_cuda_error.load(); }
 
+int attn_debug_exp2(const float *x, float *y, long long n, int poly, attn_stream_t stream) {
+  if (n < 0 || (poly != 0 && poly != 1)) return ATTN_ERR_INVALID_ARG;
+  if (n == 0) return ATTN_OK;
+  if (!x || !y) return ATTN_ERR_INVALID_ARG;
+  cudaError_t e = seqattn::launch_exp2_probe(x, y, n, poly != 0, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
 int attn_debug_expire_wait(unsigned timeout_us, attn_stream_t stream) {
   if (timeout_us == 0 || timeout_us > 1000000u) return ATTN_ERR_INVALID_ARG;
   cudaError_t e = seqattn::launch_expire_wait(timeout_us, reinterpret_cast<cudaStream_t>(stream));

@@ -93,7 +93,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (!any) {
       for (int g = 0; g < 2; ++g)
         write_empty_rows<kD, kF32Out>(p, bh, row0 + 256 * g + kRowsPerTile * static_cast<int>(rank),
-                                      kRowsPerTile);
+                                      kRowsPerTile, threadIdx.x, blockDim.x);
       return;
     }
   }
@@ -253,7 +253,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t pfull_local = bar(kBarPFull + g);
     const uint32_t pfull_leader = mapa_shared(pfull_local, 0);
     softmax_row<kD, kF32Out>(p, row, tile_first, g ? n_grp[1] : n_grp[0], tS(g) + lane_off,
-                             tO(g) + lane_off, bar(kBarSFull + g), bar(kBarOFull + g),
+                             tO(g) + lane_off, bar(kBarSFull + g), bar(kBarOFull + g), 0, 0u,
                              static_cast<size_t>(bh) * p.Sq + row, abort_flag, err,
                              EpilogueStore{nullptr, 0u, 0, 0}, [&] {
                                __syncwarp();

@@ -44,6 +44,52 @@ __device__ __forceinline__ float row_max(const float *s) {
   return fmax3(fmaxf(a, b), c, d);
 }
 
+// 2^x for a pair of floats on the FMA pipe, offloading the MUFU unit (whose
+// ex2 rate, 16 results per clock per SM, otherwise bounds the softmax):
+// Cody-Waite style range reduction x = j + f with j = rint(x), found by adding
+// and subtracting 1.5 * 2^23 (round-to-nearest), and f in [-1/2, 1/2]; 2^f by
+// a degree-3 polynomial with p(0) = 1 whose other coefficients were fitted
+// for least maximum relative error on [-1/2, 1/2] (a linear program on a
+// dense grid, 1.0e-4 in fp32 Horner form, far below the bf16 rounding of P);
+// 2^j enters by adding j to the exponent field (the low bits of 1.5*2^23 + j,
+// shifted by 23, are j << 23). x is clamped at -127 first: then every result
+// is a non-negative float, and x = -inf gives +0 exactly (j = -127, f = 0,
+// p = 1). Valid for x <= 127.
+constexpr float kExp2C1 = 0x1.62f5fap-1f;
+constexpr float kExp2C2 = 0x1.f00c4cp-3f;
+constexpr float kExp2C3 = 0x1.c2a216p-5f;
+__device__ __forceinline__ uint64_t exp2_poly_x2(uint64_t x) {
+  float x0, x1;
+  f2_unpack(x, x0, x1);
+  const uint64_t xc = f2_pack(fmaxf(x0, -127.f), fmaxf(x1, -127.f));
+  const uint64_t magic = f2_pack(12582912.f, 12582912.f);  // 1.5 * 2^23
+  const uint64_t t = f2_add(xc, magic);                      // 1.5 * 2^23 + j
+  const uint64_t j = f2_add(t, f2_pack(-12582912.f, -12582912.f));
+  const uint64_t f = f2_fma(j, f2_pack(-1.f, -1.f), xc);    // x - j, exact
+  uint64_t p = f2_fma(f, f2_pack(kExp2C3, kExp2C3), f2_pack(kExp2C2, kExp2C2));
+  p = f2_fma(p, f, f2_pack(kExp2C1, kExp2C1));
+  p = f2_fma(p, f, f2_pack(1.f, 1.f));
+  float p0, p1, t0, t1;
+  f2_unpack(p, p0, p1);
+  f2_unpack(t, t0, t1);
+  return f2_pack(__uint_as_float(__float_as_uint(p0) + (__float_as_uint(t0) << 23)),
+                 __uint_as_float(__float_as_uint(p1) + (__float_as_uint(t1) << 23)));
+}
+
+// Of every 8 pairs of a row's exponentials, this many take exp2_poly_x2 and
+// the rest the MUFU ex2.
+#ifndef SEQATTN_POLY_EXP_PAIRS_PER_8
+#define SEQATTN_POLY_EXP_PAIRS_PER_8 2
+#endif
+constexpr int kPolyExpPairsPer8 = SEQATTN_POLY_EXP_PAIRS_PER_8;
+
+__device__ __forceinline__ uint64_t exp2_pair(uint64_t x, bool poly) {
+  if (poly) return exp2_poly_x2(x);
+  float a, b;
+  f2_unpack(x, a, b);
+  return f2_pack(ex2_approx(a), ex2_approx(b));
+}
+
 // P = 2^(s * c2 - m_ref) for the 128 scores of a row, packed as bf16 pairs
 // (element 2i in the low half), returning the fp32 sum of the unrounded P.
 // With kTrackMax the raw row maximum is found in the same pass.
@@ -55,22 +101,24 @@ __device__ __forceinline__ float exp_row(const float *s, float c2, float m_ref, 
   uint64_t sum_a = f2_pack(0.f, 0.f), sum_b = sum_a;
   float ma = -INFINITY, mb = -INFINITY;
 #pragma unroll
-  for (int c = 0; c < 64; c += 2) {
-    float x0, x1, x2, x3;
-    f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), scale2, neg_m2), x0, x1);
-    f2_unpack(f2_fma(f2_pack(s[2 * c + 2], s[2 * c + 3]), scale2, neg_m2), x2, x3);
-    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-    const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
-    sum_a = f2_add(sum_a, f2_pack(p0, p1));
-    sum_b = f2_add(sum_b, f2_pack(p2, p3));
+  for (int q = 0; q < 64; q += 2) {  // pairs q and q + 1: elements 2q .. 2q + 3
+    const uint64_t pa = exp2_pair(f2_fma(f2_pack(s[2 * q], s[2 * q + 1]), scale2, neg_m2),
+                                  (q % 8) < kPolyExpPairsPer8);
+    const uint64_t pb = exp2_pair(f2_fma(f2_pack(s[2 * q + 2], s[2 * q + 3]), scale2, neg_m2),
+                                  ((q + 1) % 8) < kPolyExpPairsPer8);
+    sum_a = f2_add(sum_a, pa);
+    sum_b = f2_add(sum_b, pb);
     if (kTrackMax) {
-      ma = fmax3(ma, s[2 * c], s[2 * c + 1]);
-      mb = fmax3(mb, s[2 * c + 2], s[2 * c + 3]);
+      ma = fmax3(ma, s[2 * q], s[2 * q + 1]);
+      mb = fmax3(mb, s[2 * q + 2], s[2 * q + 3]);
     }
+    float p0, p1, p2, p3;
+    f2_unpack(pa, p0, p1);
+    f2_unpack(pb, p2, p3);
     __nv_bfloat162 h0 = __floats2bfloat162_rn(p0, p1);
     __nv_bfloat162 h1 = __floats2bfloat162_rn(p2, p3);
-    pk[c] = *reinterpret_cast<uint32_t *>(&h0);
-    pk[c + 1] = *reinterpret_cast<uint32_t *>(&h1);
+    pk[q] = *reinterpret_cast<uint32_t *>(&h0);
+    pk[q + 1] = *reinterpret_cast<uint32_t *>(&h1);
   }
   if (kTrackMax) *mx_out = fmaxf(ma, mb);
   float a0, a1, b0, b1;
@@ -82,18 +130,19 @@ __device__ __forceinline__ float exp_row(const float *s, float c2, float m_ref, 
 
 // A block of query rows none of which sees a key: lse = -inf and, unless the
 // caller asked to skip them, O = 0. The rows of one head are contiguous in
-// memory, so the zero fill is one coalesced run of 16-byte stores by the CTA.
+// memory, so the zero fill is one coalesced run of 16-byte stores by the
+// `nthreads` threads taking part (tid = 0 .. nthreads - 1).
 template <int D, bool kF32Out>
 __device__ __forceinline__ void write_empty_rows(const AttnParams &p, int bh, int row_begin,
-                                                 int nrows) {
+                                                 int nrows, int tid, int nthreads) {
   const int rows = min(nrows, p.Sq - row_begin);
   if (rows <= 0) return;
   const size_t base = static_cast<size_t>(bh) * p.Sq + row_begin;
-  for (int i = threadIdx.x; i < rows; i += blockDim.x) p.lse[base + i] = -INFINITY;
+  for (int i = tid; i < rows; i += nthreads) p.lse[base + i] = -INFINITY;
   if (p.skip_empty) return;
   const size_t n16 = static_cast<size_t>(rows) * D * (kF32Out ? 4 : 2) / 16;
   uint4 *dst = reinterpret_cast<uint4 *>(static_cast<char *>(p.o) + base * D * (kF32Out ? 4 : 2));
-  for (size_t i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (size_t i = tid; i < n16; i += nthreads) dst[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
 // How a warpgroup's epilogue writes its 128-row O tile. With a tensor map the
@@ -104,8 +153,7 @@ __device__ __forceinline__ void write_empty_rows(const AttnParams &p, int bh, in
 // thread stores its own row.
 struct EpilogueStore {
   const CUtensorMap *map;  // O as [heads][rows][D], box 128 bytes x 128 rows x 1, 128-byte swizzle
-  uint32_t stage;          // shared address of D/64 staging boxes of 16 KB, 1024-byte aligned,
-                           // free once this tile's final O is signalled
+  uint32_t stage;          // shared address of this warpgroup's 16 KB staging box (1024-byte aligned)
   int named_bar;           // barrier id private to the warpgroup (128 threads)
   int head;                // third map coordinate, b * Hq + hq
 };
@@ -117,10 +165,15 @@ struct EpilogueStore {
 //                     mbarriers the MMA issuer commits when S(j) / the final O
 //                     are ready; signal_p() tells it P(j) is in TMEM (called by
 //                     every thread after its tcgen05 stores are fenced).
+//   step_base         S(j) completes phase step_base + j of bar_sfull (a CTA
+//                     that works through several tiles keeps counting)
+//   ofull_parity      parity of the bar_ofull phase that marks this tile's O
+// Returns false if the pipeline was aborted.
 template <int D, bool kF32Out, typename SignalP>
-__device__ __forceinline__ void softmax_row(const AttnParams &p, int row, int tile_first_row, int n,
+__device__ __forceinline__ bool softmax_row(const AttnParams &p, int row, int tile_first_row, int n,
                                             uint32_t s_addr, uint32_t o_addr, uint32_t bar_sfull,
-                                            uint32_t bar_ofull, size_t row_index,
+                                            uint32_t bar_ofull, int step_base,
+                                            uint32_t ofull_parity, size_t row_index,
                                             volatile int *abort_flag, int *err,
                                             const EpilogueStore &store, SignalP signal_p) {
     const long long qpos = p.q_off + row;
@@ -132,7 +185,8 @@ __device__ __forceinline__ void softmax_row(const AttnParams &p, int row, int ti
     bool ok = true;
 
     for (int j = 0; j < n; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_sfull, j & 1, abort_flag, err));
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(bar_sfull, static_cast<uint32_t>(step_base + j) & 1u, abort_flag, err));
       if (!ok) break;
       tc_fence_after();
       const int kv0 = j * kRowsPerTile;
@@ -215,7 +269,7 @@ __device__ __forceinline__ void softmax_row(const AttnParams &p, int row, int ti
     // ------------------------------------------------------------ epilogue
     bool have_o = false;
     if (ok && n > 0) {
-      have_o = __all_sync(0xffffffffu, mbar_wait(bar_ofull, 0, abort_flag, err));
+      have_o = __all_sync(0xffffffffu, mbar_wait(bar_ofull, ofull_parity, abort_flag, err));
       tc_fence_after();
     }
     const bool row_valid = row < p.Sq;
@@ -232,7 +286,6 @@ __device__ __forceinline__ void softmax_row(const AttnParams &p, int row, int ti
     if (via_tma) {
       constexpr int kChunkCols = kF32Out ? 32 : 64;  // 128 bytes of a row
       constexpr int kChunks = D / kChunkCols;
-      constexpr int kBufs = D / 64;
       const bool leader = (threadIdx.x & 127) == 0;
       const uint32_t row_in_tile = static_cast<uint32_t>(row - tile_first_row);
       const uint32_t swz = row_in_tile & 7u;
@@ -258,10 +311,10 @@ __device__ __forceinline__ void softmax_row(const AttnParams &p, int row, int ti
             }
           }
         }
-        const uint32_t buf = store.stage + static_cast<uint32_t>(c % kBufs) * 16384u;
-        if (c >= kBufs) {
-          // the box stored from this buffer kBufs chunks ago must have been read
-          if (leader) bulk_wait_group_read<kBufs - 1>();
+        const uint32_t buf = store.stage;
+        if (c > 0) {
+          // the previous chunk's box must have been read out of the buffer
+          if (leader) bulk_wait_group_read<0>();
           __syncwarp();
           named_bar_sync(store.named_bar, 128);
         }
@@ -278,11 +331,11 @@ __device__ __forceinline__ void softmax_row(const AttnParams &p, int row, int ti
           bulk_commit_group();
         }
       }
-      // The staging boxes are shared memory of this CTA: every store must be
-      // complete before the CTA may exit.
-      if (leader) bulk_wait_all();
+      // The staging box is reused by the next tile and freed when the CTA
+      // exits: the last store must have read it.
+      if (leader) bulk_wait_group_read<0>();
       if (row_valid) p.lse[row_index] = (l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
-      return;
+      return true;  // every thread of the warpgroup had the final O
     }
 #pragma unroll 1
     for (int cb = 0; cb < D / 32; ++cb) {
@@ -319,6 +372,10 @@ __device__ __forceinline__ void softmax_row(const AttnParams &p, int row, int ti
       }
     }
     if (row_valid) p.lse[row_index] = (l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
+    const bool done = ok && (n == 0 || have_o);
+    // a caller that goes on to another tile needs the same answer on every
+    // thread of the warpgroup
+    return store.map != nullptr ? named_bar_and(store.named_bar, 128, done) : done;
 }
 
 }  // namespace detail

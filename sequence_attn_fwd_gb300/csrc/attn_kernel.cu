@@ -32,6 +32,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "attn_common.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -55,10 +57,37 @@ struct Cfg {
   static constexpr int kStages = (D == 128) ? 4 : 8;
   static constexpr int kSmemQ = 2 * kTileBytes;
   static constexpr int kSmemRing = kStages * kTileBytes;
-  // barriers: q, full[S], empty[S], s_full[2], p_full[2], o_full[2], mma_done
-  static constexpr int kNumBarriers = 1 + 2 * kStages + 7;
-  static constexpr int kSmemBytes = 1024 + kSmemQ + kSmemRing + 8 * kNumBarriers + 16;
+  static constexpr int kStageBytes = 16384;  // epilogue staging box of one softmax warpgroup
+  static constexpr int kSmemStage = 2 * kStageBytes;
+  // barriers: q_full, q_empty, full[S], empty[S], s_full[2], p_full[2], o_full[2], mma_done
+  static constexpr int kNumBarriers = 2 + 2 * kStages + 7;
+  static constexpr int kSmemBytes =
+      1024 + kSmemQ + kSmemRing + kSmemStage + 8 * kNumBarriers + 16;
 };
+static_assert(Cfg<128>::kSmemBytes <= 232448 && Cfg<64>::kSmemBytes <= 232448,
+              "shared memory per CTA");
+
+// Work item k of a launch: a block of 256 query rows of one (batch, head).
+// Items are numbered with the head fastest; causal launches number the longest
+// query blocks (most KV tiles) first.
+struct Item {
+  int bh;    // b * Hq + hq
+  int row0;  // first query row of the block
+};
+// The i-th item of this CTA. Items are dealt in rounds of gridDim.x, one per
+// CTA, in alternating direction, so that with causal cost falling along the
+// numbering every CTA's total stays within one item of every other's.
+__device__ __forceinline__ long long item_index(long long i) {
+  const long long G = gridDim.x;
+  return i * G + ((i & 1) ? (G - 1 - blockIdx.x) : blockIdx.x);
+}
+__device__ __forceinline__ Item item_of(const AttnParams &p, long long k) {
+  const long long heads = static_cast<long long>(p.B) * p.Hq;
+  const int qi = static_cast<int>(k / heads);
+  const int qblock = p.causal ? p.n_qblocks - 1 - qi : qi;
+  return {static_cast<int>(k % heads), qblock * 2 * kRowsPerTile};
+}
+
 template <int D, bool kF32Out>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -69,37 +98,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
-  uint8_t *sQ = smem;                   // [tile][col block][128 rows][128 B]
-  uint8_t *sRing = smem + C::kSmemQ;    // [slot][col block][128 rows][128 B]
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sRing + C::kSmemRing);
+  uint8_t *sQ = smem;                          // [tile][col block][128 rows][128 B]
+  uint8_t *sRing = smem + C::kSmemQ;           // [slot][col block][128 rows][128 B]
+  uint8_t *sStage = sRing + C::kSmemRing;      // [warpgroup][16 KB]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sStage + C::kSmemStage);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kNumBarriers);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const uint32_t bar0 = smem_addr(bars);
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
-  const int kBarQ = 0, kBarFull = 1, kBarEmpty = 1 + C::kStages, kBarSFull = 1 + 2 * C::kStages,
-            kBarPFull = kBarSFull + 2, kBarOFull = kBarPFull + 2, kBarMmaDone = kBarOFull + 2;
+  const int kBarQFull = 0, kBarQEmpty = 1, kBarFull = 2, kBarEmpty = 2 + C::kStages,
+            kBarSFull = 2 + 2 * C::kStages, kBarPFull = kBarSFull + 2, kBarOFull = kBarPFull + 2,
+            kBarMmaDone = kBarOFull + 2;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;  // b * Hq + hq: heads of one GQA group are neighbours
-  const int b = bh / p.Hq, hq = bh % p.Hq;
-  const int hkv = hq / (p.Hq / p.Hkv);
-  // causal: the longest query blocks (most KV tiles) are launched first
-  const int qblock = p.causal ? (p.n_qblocks - 1 - static_cast<int>(blockIdx.y))
-                              : static_cast<int>(blockIdx.y);
-  const int row0 = qblock * 2 * kRowsPerTile;
   int *err = &g_device_error;
-
-  // No row of this block sees a key (rows past the end, or a causal chunk that
-  // lies entirely after them): no pipeline needed.
-  if (kv_tiles_for(p, row0) == 0 && kv_tiles_for(p, row0 + kRowsPerTile) == 0) {
-    write_empty_rows<D, kF32Out>(p, bh, row0, 2 * kRowsPerTile);
-    return;
-  }
+  const long long n_items = static_cast<long long>(p.B) * p.Hq * p.n_qblocks;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(kBarQ), 1);
+    mbar_init(bar(kBarQFull), 1);
+    mbar_init(bar(kBarQEmpty), 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bar(kBarFull + s), 1);
       mbar_init(bar(kBarEmpty + s), 1);
@@ -125,97 +144,138 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const bool skip = *abort_flag != 0;
-  const int n_tiles[2] = {skip ? 0 : kv_tiles_for(p, row0), skip ? 0 : kv_tiles_for(p, row0 + kRowsPerTile)};
-  const int n_max = max(n_tiles[0], n_tiles[1]);
+  // KV tiles query tile t of an item visits (0: none of its rows sees a key)
+  auto tiles = [&](const Item &it, int t) -> int {
+    return skip ? 0 : kv_tiles_for(p, it.row0 + t * kRowsPerTile);
+  };
   // TMEM column of S_t / P_t and of O_t for query tile t
   auto tS = [&](int t) -> uint32_t { return tmem + 128u * static_cast<uint32_t>(t); };
   auto tO = [&](int t) -> uint32_t { return tmem + 256u + 128u * static_cast<uint32_t>(t); };
 
+  // The CTA works through items item_index(0), item_index(1), ...; each role
+  // walks the same sequence and skips the items with no visible key.
+  // Barrier phases run on across items: the Q buffer by loaded item, the K/V
+  // ring by ring position, S/P by KV step of each query tile, O by item of
+  // each query tile.
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_max > 0) {
+    if (lane == 0 && !skip) {
       tma_prefetch_map(&tm_q);
       tma_prefetch_map(&tm_k);
       tma_prefetch_map(&tm_v);
-      mbar_arrive_expect_tx(bar(kBarQ), 2 * C::kTileBytes);
-      for (int t = 0; t < 2; ++t)
-        for (int cb = 0; cb < C::kColBlocks; ++cb)
-          tma_load_3d(smem_addr(sQ + (t * C::kColBlocks + cb) * kColBlockBytes), &tm_q, bar(kBarQ),
-                      cb * 64, row0 + t * kRowsPerTile, bh);
-      const int kv_head = b * p.Hkv + hkv;
-      int c = 0;  // K_0, V_0, K_1, V_1, ... in the order the MMA issuer consumes them
+      int c = 0;   // K_0, V_0, K_1, V_1, ... of every item, in the order the MMA issuer consumes them
+      int nq = 0;  // Q tile pairs loaded
       bool ok = true;
-      for (int j = 0; j < n_max && ok; ++j) {
-        for (int which = 0; which < 2; ++which, ++c) {
-          const int slot = c % C::kStages;
-          if (c >= C::kStages &&
-              !mbar_wait(bar(kBarEmpty + slot), ((c / C::kStages) - 1) & 1, abort_flag, err)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(bar(kBarFull + slot), C::kTileBytes);
-          const CUtensorMap *map = which ? &tm_v : &tm_k;
+      for (long long i = 0, k = item_index(0); k < n_items && ok; k = item_index(++i)) {
+        const Item it = item_of(p, k);
+        const int n_max = max(tiles(it, 0), tiles(it, 1));
+        if (n_max == 0) continue;
+        // the previous item's S MMAs must be done reading the Q buffer
+        if (nq > 0 && !mbar_wait(bar(kBarQEmpty), (nq - 1) & 1, abort_flag, err)) break;
+        mbar_arrive_expect_tx(bar(kBarQFull), 2 * C::kTileBytes);
+        for (int t = 0; t < 2; ++t)
           for (int cb = 0; cb < C::kColBlocks; ++cb)
-            tma_load_3d(smem_addr(sRing + (slot * C::kColBlocks + cb) * kColBlockBytes), map,
-                        bar(kBarFull + slot), cb * 64, j * kRowsPerTile, kv_head);
+            tma_load_3d(smem_addr(sQ + (t * C::kColBlocks + cb) * kColBlockBytes), &tm_q,
+                        bar(kBarQFull), cb * 64, it.row0 + t * kRowsPerTile, it.bh);
+        ++nq;
+        const int b = it.bh / p.Hq, hq = it.bh % p.Hq;
+        const int kv_head = b * p.Hkv + hq / (p.Hq / p.Hkv);
+        for (int j = 0; j < n_max && ok; ++j) {
+          for (int which = 0; which < 2; ++which, ++c) {
+            const int slot = c % C::kStages;
+            if (c >= C::kStages &&
+                !mbar_wait(bar(kBarEmpty + slot), ((c / C::kStages) - 1) & 1, abort_flag, err)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar(kBarFull + slot), C::kTileBytes);
+            const CUtensorMap *map = which ? &tm_v : &tm_k;
+            for (int cb = 0; cb < C::kColBlocks; ++cb)
+              tma_load_3d(smem_addr(sRing + (slot * C::kColBlocks + cb) * kColBlockBytes), map,
+                          bar(kBarFull + slot), cb * 64, j * kRowsPerTile, kv_head);
+          }
         }
       }
-      // Every copy issued must have landed before the CTA may exit.
-      mbar_drain(bar(kBarQ), 0, err);
+      // Every copy issued must have landed before the CTA may exit (only the
+      // last Q load and the last ring fills can still be in flight).
+      if (nq > 0) mbar_drain(bar(kBarQFull), (nq - 1) & 1, err);
       for (int i = max(0, c - C::kStages); i < c; ++i)
         mbar_drain(bar(kBarFull + i % C::kStages), (i / C::kStages) & 1, err);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && !skip) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, true);
       const uint32_t q_base = smem_addr(sQ);
       const uint32_t ring_base = smem_addr(sRing);
-      bool ok = n_max > 0 && mbar_wait(bar(kBarQ), 0, abort_flag, err);
-      // Per KV step j: PV_0(j-1), S_0(j), PV_1(j-1), S_1(j). Both ring slots of
-      // the step are waited for first (measured faster on GB300 than waiting
-      // for each just before its first use); each slot is released by a commit
-      // that fires when its last MMA completes.
-      for (int j = 0; ok && j <= n_max; ++j) {
-        const int cK = 2 * j, cV = 2 * j - 1;  // ring positions of K_j and V_{j-1}
-        const int sK = cK % C::kStages, sV = (cV + C::kStages) % C::kStages;
-        const uint32_t k_base = ring_base + sK * C::kTileBytes;
-        const uint32_t v_base = ring_base + sV * C::kTileBytes;
-        if (j < n_max && !mbar_wait(bar(kBarFull + sK), (cK / C::kStages) & 1, abort_flag, err)) break;
-        if (j >= 1 && !mbar_wait(bar(kBarFull + sV), (cV / C::kStages) & 1, abort_flag, err)) break;
-        tc_fence_after();
-        for (int t = 0; t < 2 && ok; ++t) {
-          const int nt = t ? n_tiles[1] : n_tiles[0];
-          if (j >= 1 && j - 1 < nt) {
-            // O_t += P_t V_{j-1}; P_t was written over S_t by the softmax warps
-            if (!mbar_wait(bar(kBarPFull + t), (j - 1) & 1, abort_flag, err)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < kRowsPerTile / 16; ++kk) {
-              const uint64_t bdesc = sw128_desc(v_base + kk * 2048, kColBlockBytes, 1024);
-              mma_ts(tO(t), tS(t) + kk * 8, bdesc, idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
-            }
-            if (j - 1 == nt - 1) mma_commit(bar(kBarOFull + t));
-            if (t == 1 || j - 1 >= n_tiles[1]) mma_commit(bar(kBarEmpty + sV));  // last use of V_{j-1}
+      int c = 0;             // ring position of the item's K_0
+      int nq = 0;            // Q tile pairs consumed
+      int g[2] = {0, 0};     // KV steps done by each query tile over earlier items
+      bool ok = true;
+      for (long long i = 0, k = item_index(0); k < n_items && ok; k = item_index(++i)) {
+        const Item it = item_of(p, k);
+        const int n_t[2] = {tiles(it, 0), tiles(it, 1)};
+        const int n_max = max(n_t[0], n_t[1]);
+        if (n_max == 0) continue;
+        if (!mbar_wait(bar(kBarQFull), nq & 1, abort_flag, err)) break;
+        ++nq;
+        // Per KV step j: PV_0(j-1), S_0(j), PV_1(j-1), S_1(j). Both ring slots
+        // of the step are waited for first; each slot is released by a commit
+        // that fires when its last MMA completes.
+        for (int j = 0; ok && j <= n_max; ++j) {
+          const int cK = c + 2 * j, cV = c + 2 * j - 1;  // ring positions of K_j and V_{j-1}
+          const int sK = cK % C::kStages, sV = (cV + C::kStages) % C::kStages;
+          const uint32_t k_base = ring_base + sK * C::kTileBytes;
+          const uint32_t v_base = ring_base + sV * C::kTileBytes;
+          if (j < n_max && !mbar_wait(bar(kBarFull + sK), (cK / C::kStages) & 1, abort_flag, err)) {
+            ok = false;
+            break;
           }
-          if (j < nt) {
-            // S_t = Q_t K_j^T
-            const uint32_t qt = q_base + t * C::kTileBytes;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk / 4) * kColBlockBytes + (kk % 4) * 32;
-              mma_ss(tS(t), sw128_desc(qt + off, 16, 1024), sw128_desc(k_base + off, 16, 1024),
-                     idesc_s, kk > 0 ? 1u : 0u);
-            }
-            mma_commit(bar(kBarSFull + t));
-            if (t == 1 || j >= n_tiles[1]) mma_commit(bar(kBarEmpty + sK));  // last use of K_j
+          if (j >= 1 && !mbar_wait(bar(kBarFull + sV), (cV / C::kStages) & 1, abort_flag, err)) {
+            ok = false;
+            break;
           }
+          tc_fence_after();
+          for (int t = 0; t < 2 && ok; ++t) {
+            const int nt = n_t[t];
+            if (j >= 1 && j - 1 < nt) {
+              // O_t += P_t V_{j-1}; P_t was written over S_t by the softmax
+              // warps. For j = 1 this overwrites O_t: the warpgroup read the
+              // previous item's O_t before it signalled this P.
+              if (!mbar_wait(bar(kBarPFull + t), (g[t] + j - 1) & 1, abort_flag, err)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < kRowsPerTile / 16; ++kk) {
+                const uint64_t bdesc = sw128_desc(v_base + kk * 2048, kColBlockBytes, 1024);
+                mma_ts(tO(t), tS(t) + kk * 8, bdesc, idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
+              }
+              if (j - 1 == nt - 1) mma_commit(bar(kBarOFull + t));
+              if (t == 1 || j - 1 >= n_t[1]) mma_commit(bar(kBarEmpty + sV));  // last use of V_{j-1}
+            }
+            if (j < nt) {
+              // S_t = Q_t K_j^T
+              const uint32_t qt = q_base + t * C::kTileBytes;
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk / 4) * kColBlockBytes + (kk % 4) * 32;
+                mma_ss(tS(t), sw128_desc(qt + off, 16, 1024), sw128_desc(k_base + off, 16, 1024),
+                       idesc_s, kk > 0 ? 1u : 0u);
+              }
+              mma_commit(bar(kBarSFull + t));
+              if (t == 1 || j >= n_t[1]) mma_commit(bar(kBarEmpty + sK));  // last use of K_j
+            }
+          }
+          // every S MMA of the item is issued: the Q buffer is free once they complete
+          if (ok && j == n_max - 1) mma_commit(bar(kBarQEmpty));
         }
+        c += 2 * n_max;
+        g[0] += n_t[0];
+        g[1] += n_t[1];
       }
       // All MMAs issued here must be complete before TMEM is released.
       mma_commit(bar(kBarMmaDone));
@@ -226,19 +286,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ softmax + epilogue
     const int t = warp >> 2;                         // query tile of this warpgroup
     const int row_in_tile = (warp & 3) * 32 + lane;  // TMEM lane = tile row
-    const int row = row0 + t * kRowsPerTile + row_in_tile;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t pfull = bar(kBarPFull + t);
-    // Query tile t's shared memory is free once O_t is final: every S_t MMA
-    // was issued before the last PV_t MMA, and MMAs complete in issue order.
-    const EpilogueStore store{&tm_o, smem_addr(sQ + t * C::kTileBytes), 1 + t, bh};
-    softmax_row<D, kF32Out>(p, row, row0 + t * kRowsPerTile, t ? n_tiles[1] : n_tiles[0],
-                            tS(t) + lane_off, tO(t) + lane_off, bar(kBarSFull + t),
-                            bar(kBarOFull + t), static_cast<size_t>(bh) * p.Sq + row, abort_flag, err,
-                            store, [&] {
-                              __syncwarp();
-                              if (lane == 0) mbar_arrive(pfull);  // one arrival per warp
-                            });
+    const uint32_t stage = smem_addr(sStage + t * C::kStageBytes);
+    int g = 0;       // KV steps of this tile over earlier items
+    uint32_t u = 0;  // earlier items in which this tile visited a KV tile
+    for (long long i = 0, k = item_index(0); k < n_items; k = item_index(++i)) {
+      const Item it = item_of(p, k);
+      const int tile_first = it.row0 + t * kRowsPerTile;
+      const int n = tiles(it, t);
+      if (n == 0) {
+        write_empty_rows<D, kF32Out>(p, it.bh, tile_first, kRowsPerTile, threadIdx.x & 127, 128);
+        continue;
+      }
+      const int row = tile_first + row_in_tile;
+      const EpilogueStore store{&tm_o, stage, 1 + t, it.bh};
+      const bool ok = softmax_row<D, kF32Out>(
+          p, row, tile_first, n, tS(t) + lane_off, tO(t) + lane_off, bar(kBarSFull + t),
+          bar(kBarOFull + t), g, u & 1u, static_cast<size_t>(it.bh) * p.Sq + row, abort_flag,
+          err, store, [&] {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pfull);  // one arrival per warp
+          });
+      g += n;
+      ++u;
+      if (!ok) break;  // the same on every thread of the warpgroup
+    }
   }
 
   tc_fence_before();
@@ -249,6 +322,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Number of SMs of the current device (read once per device).
+int sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev >= 0 && dev < 64) {
+    const int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 1;
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
 template <int D, bool kF32Out>
 cudaError_t launch_typed(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                          const CUtensorMap &to, const AttnParams &p, cudaStream_t stream) {
@@ -256,8 +345,10 @@ cudaError_t launch_typed(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg<D>::kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(static_cast<unsigned>(p.B * p.Hq), static_cast<unsigned>(p.n_qblocks));
-  kernel<<<grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, to, p);
+  // persistent: one CTA per SM (or per work item, if there are fewer)
+  const long long n_items = static_cast<long long>(p.B) * p.Hq * p.n_qblocks;
+  const long long grid = n_items < sm_count() ? n_items : sm_count();
+  kernel<<<static_cast<unsigned>(grid), kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
@@ -307,6 +398,26 @@ __global__ void expire_wait_kernel(unsigned long long limit_ns) {
 
 cudaError_t launch_expire_wait(unsigned timeout_us, cudaStream_t stream) {
   expire_wait_kernel<<<1, 32, 0, stream>>>(static_cast<unsigned long long>(timeout_us) * 1000ull);
+  return cudaGetLastError();
+}
+
+// Element pairs (2i, 2i + 1) through exp2_pair; an odd last element pairs with itself.
+__global__ void exp2_probe_kernel(const float *x, float *y, long long n, bool poly) {
+  const long long i = 2 * (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x);
+  if (i >= n) return;
+  const float a = x[i], b = (i + 1 < n) ? x[i + 1] : a;
+  float ra, rb;
+  f2_unpack(exp2_pair(f2_pack(a, b), poly), ra, rb);
+  y[i] = ra;
+  if (i + 1 < n) y[i + 1] = rb;
+}
+
+cudaError_t launch_exp2_probe(const float *x, float *y, long long n, bool poly,
+                              cudaStream_t stream) {
+  const long long pairs = (n + 1) / 2;
+  const long long blocks = (pairs + 255) / 256;
+  if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
+  exp2_probe_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, y, n, poly);
   return cudaGetLastError();
 }
 

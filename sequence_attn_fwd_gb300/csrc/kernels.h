@@ -37,6 +37,10 @@ cudaError_t launch_lse_merge(const float *o_parts, const float *lse_parts, int P
 // One CTA waits on an mbarrier nothing arrives at until timeout_us runs out.
 cudaError_t launch_expire_wait(unsigned timeout_us, cudaStream_t stream);
 
+// y[i] = 2^x[i] by the softmax's exponential routine (polynomial or MUFU).
+cudaError_t launch_exp2_probe(const float *x, float *y, long long n, bool poly,
+                              cudaStream_t stream);
+
 // Reads and clears the device error word (after the caller synchronised).
 cudaError_t read_and_clear_device_error(int *code);
 

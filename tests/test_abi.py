@@ -31,7 +31,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted(["attn_fwd", "attn_partial", "lse_merge", "attn_query_device_error",
                                            "attn_status_string", "attn_last_cuda_error",
-                                           "attn_ring_fwd_static", "attn_debug_expire_wait"])
+                                           "attn_ring_fwd_static", "attn_debug_expire_wait",
+                                           "attn_debug_exp2"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -51,6 +52,13 @@ def test_library_is_built_for_sm103a():
 def test_expire_wait_argument_checks(lib):
     assert lib.attn_debug_expire_wait(0, None) == 1
     assert lib.attn_debug_expire_wait(2_000_000, None) == 1
+
+
+def test_exp2_hook_argument_checks(lib):
+    assert lib.attn_debug_exp2(FAKE, FAKE, -1, 1, None) == 1
+    assert lib.attn_debug_exp2(FAKE, FAKE, 4, 2, None) == 1
+    assert lib.attn_debug_exp2(0, FAKE, 4, 1, None) == 1
+    assert lib.attn_debug_exp2(0, 0, 0, 0, None) == 0
 
 
 def test_status_strings(lib):

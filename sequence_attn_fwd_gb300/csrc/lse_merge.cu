@@ -91,8 +91,14 @@ __global__ void __launch_bounds__(kMergeThreads)
   }
 }
 
+// Up to 8 parts a row carries few loads, so more rows are kept in flight:
+// four per warp step and three CTAs per SM (measured best on GB300 for 8
+// parts; two and two for 16).
+template <int kPMax>
+constexpr int rows32_min_blocks() { return kPMax <= 8 ? 3 : 2; }
+
 template <int D, bool kBf16Out, int kPMax>
-__global__ void __launch_bounds__(kMergeThreads, 2)
+__global__ void __launch_bounds__(kMergeThreads, rows32_min_blocks<kPMax>())
     lse_merge_rows32_kernel(const float *o_parts, const float *lse_parts, int P, long long nrows,
                             void *o_out, float *lse_out) {
   constexpr int kSlots = D / 4;            // float4 slices per row
@@ -126,8 +132,8 @@ __global__ void __launch_bounds__(kMergeThreads, 2)
     // all of this row's lse_parts are in registers before the (possibly aliased) write
     if (my_valid) lse_out[my_row] = (mx == -INFINITY) ? -INFINITY : mx + logf(wsum);
 
-    // the 32 rows' outputs: D/4 lanes per row (two rows' loads in flight when P is small)
-#pragma unroll(kPMax <= 16 ? 2 : 1)
+    // the 32 rows' outputs: D/4 lanes per row (several rows' loads in flight when P is small)
+#pragma unroll(kPMax <= 8 ? 4 : (kPMax <= 16 ? 2 : 1))
     for (int r = 0; r < 32; r += kRowsPerStep) {
       const int rr = r + rsub;
       const long long row = base + rr;

@@ -187,9 +187,12 @@ def test_lse_merge_on_synthetic_partials(sa, D, causal_pattern):
     check_lse(lp[0], lse_ref, tol=1e-5)
 
 
-@pytest.mark.parametrize("P", [1, 2, 5, 33])
-def test_lse_merge_part_counts(sa, P):
-    o_parts, lse_parts = workloads.make_partials(P, 1, 2, 130, 128, seed=40 + P, causal=False)
+@pytest.mark.parametrize("P,D", [(1, 128), (2, 128), (5, 128), (32, 128), (33, 128), (3, 64), (32, 64),
+                                 (64, 64)])
+def test_lse_merge_part_counts(sa, P, D):
+    """Both merge paths (bulk copies up to 32 parts, rows of 130 not a multiple of
+    the row group; the row kernel beyond)."""
+    o_parts, lse_parts = workloads.make_partials(P, 1, 2, 130, D, seed=40 + P, causal=False)
     o_ref, lse_ref = oracle.lse_merge(o_parts, lse_parts)
     o, l = sa.lse_merge(*to_dev(o_parts, lse_parts), out_dtype=torch.float32)
     check_o(o, o_ref, tol=1e-5, bf16_out=False)

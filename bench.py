@@ -126,6 +126,16 @@ def measured_traffic(kernel: str, workload: str, profiles_dir: str = os.path.joi
     return None
 
 
+def ring_time_from_hops(hop_ms) -> dict:
+    """Emulated ring timing from per-(hop, device) times hop_ms[t][d]: a hop
+    lasts as long as its slowest device; spread = slowest / mean device."""
+    ring = sum(max(row) for row in hop_ms)
+    busy = sum(sum(row) for row in hop_ms)
+    spread = [max(row) / (sum(row) / len(row)) if sum(row) > 0 else 1.0 for row in hop_ms]
+    return {"ring_ms": ring, "device_ms_total": busy, "hop_spread_max_over_mean": spread,
+            "balance": busy / (len(hop_ms[0]) * ring) if ring > 0 else 1.0}
+
+
 def max_over_ranks(value: float) -> float:
     import torch.distributed as dist
 
@@ -378,6 +388,37 @@ def run_reference(args, w):
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_ring_schedules(args, w: workloads.Workload) -> dict:
+    """Causal ring pass emulated device by device (each device's launches of a
+    hop timed alone: on a real ring every device is a whole GPU), for the
+    pages' contiguous layout and the zigzag one; per (hop, device) the median
+    over the timed passes."""
+    import sequence_attn_fwd_gb300 as sa
+    from sequence_attn_fwd_gb300 import ring_schedule as rs
+
+    q, k, v = (t.cuda() for t in workloads.make_qkv(w))
+    out = {}
+    for layout in rs.LAYOUTS:
+        ring = sa.EmulatedRing(q, k, v, P=w.P, layout=layout, causal=w.causal)
+        for _ in range(args.warmup):
+            ring.run()
+        # a 20 ms GPU-side hold ahead of each timed pass: the pass's launches are
+        # all enqueued before it ends, so the events time GPU work only
+        runs = [ring.run(timing=True, hold_cycles=40_000_000) for _ in range(args.steps)]
+        hop = [[statistics.median(r[0][t][d] for r in runs) for d in range(w.P)] for t in range(w.P)]
+        merge = [statistics.median(r[1][d] for r in runs) for d in range(w.P)]
+        res = ring_time_from_hops(hop)
+        res.update({"merge_ms_max_device": max(merge), "ideal_units": rs.ring_time_units(w.P, layout, w.causal),
+                    "hop_ms": [[round(x, 4) for x in row] for row in hop]})
+        out[layout] = res
+        del ring
+        torch.cuda.empty_cache()
+    return {"metric": "emulated causal ring pass: sum over hops of the slowest device's attention time",
+            "unit": "ms", "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "data": "synthetic", "config": workload_config(w), "layouts": out,
+            "speedup_zigzag": out["contiguous"]["ring_ms"] / out["zigzag"]["ring_ms"]}
+
+
 def workload_config(w: workloads.Workload):
     return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "D": w.D, "causal": w.causal,
             "P": w.P, "chunk": w.chunk, "scale": "1/sqrt(D)",
@@ -397,6 +438,9 @@ def main(argv=None):
     ap.add_argument("--cpu-baseline-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--ring-schedule", action="store_true",
+                    help="instead of the step: per-hop device times of the emulated causal ring, "
+                         "contiguous vs zigzag layout (ring workloads)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
     w = workloads.WORKLOADS[args.workload]
@@ -418,6 +462,14 @@ def main(argv=None):
     if not torch.cuda.is_available():
         print(json.dumps({"error": "no CUDA device"}))
         return 1
+    if args.ring_schedule:
+        if rank != 0:
+            return 0
+        if w.P < 2:
+            print(json.dumps({"error": "--ring-schedule needs a ring workload"}))
+            return 1
+        print(json.dumps(run_ring_schedules(args, w)), flush=True)
+        return 0
     r = run_ours(args, w, rank, world)
     if rank == 0:
         cpu = None

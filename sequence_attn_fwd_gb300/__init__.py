@@ -156,6 +156,110 @@ def ring_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, cau
     return lse_merge(o_parts, lse_parts, torch.bfloat16, out=out, lse=lse)
 
 
+class EmulatedRing:
+    """P ring devices emulated on one GPU, each with its own chunks of Q (copied
+    to device-local contiguous buffers, as each device would hold its shard) and
+    its own fp32 partials. K/V chunks are read in place (a "hop" moves no bytes
+    on one GPU). The blocks each device computes at each hop follow
+    ``ring_schedule.hop_blocks`` for the layout ("contiguous": the pages' ring,
+    one chunk per device; "zigzag": chunks d and 2P-1-d, balanced under the
+    causal mask).
+
+    run() launches, hop by hop and device by device, one attn_partial per block
+    (the query chunk's rows against the key chunk, global offsets for the
+    mask), then per query chunk one lse_merge of its partials; with timing, the
+    launches of each (hop, device) are bracketed by CUDA events. output()
+    assembles the devices' results into [B,Hq,S,D] / [B,Hq,S] (test glue)."""
+
+    def __init__(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, layout: str = "zigzag",
+                 causal: bool = True, scale: float | None = None):
+        from . import ring_schedule as rs
+
+        B, Hq, S, D = q.shape
+        nc = rs.n_chunks(P, layout)
+        _require(S % nc == 0, f"S must be a multiple of {nc} for the {layout} layout with P = {P}")
+        self.B, self.Hq, self.S, self.D, self.P, self.layout = B, Hq, S, D, P, layout
+        self.causal, self.scale, self.k, self.v = causal, scale, k, v
+        self.C = S // nc
+        self.chunks = rs.device_chunks(P, layout)
+        self.blocks = rs.hop_blocks(P, layout, causal)
+        C = self.C
+        self.q_chunk = {qc: q[:, :, qc * C:(qc + 1) * C].contiguous() for dc in self.chunks for qc in dc}
+        # partial slot of each block within its query chunk's stack, in hop order
+        self.slot, n_parts = {}, {qc: 0 for qc in self.q_chunk}
+        for hop in self.blocks:
+            for blocks in hop:
+                for b in blocks:
+                    self.slot[b] = n_parts[b.q_chunk]
+                    n_parts[b.q_chunk] += 1
+        self.o_parts = {qc: torch.empty((max(n, 1), B, Hq, C, D), dtype=torch.float32, device=q.device)
+                        for qc, n in n_parts.items()}
+        self.lse_parts = {qc: torch.empty((max(n, 1), B, Hq, C), dtype=torch.float32, device=q.device)
+                          for qc, n in n_parts.items()}
+        self.n_parts = n_parts
+        self.o = {qc: torch.empty((B, Hq, C, D), dtype=torch.bfloat16, device=q.device) for qc in self.q_chunk}
+        self.lse = {qc: torch.empty((B, Hq, C), dtype=torch.float32, device=q.device) for qc in self.q_chunk}
+
+    def run(self, timing: bool = False, hold_cycles: int = 0):
+        """One ring pass. With timing, returns ms[t][d] (the launches of device
+        d at hop t) and the merge time of each device; else None. hold_cycles
+        > 0 first queues a GPU-side wait of that many clocks, so that every
+        launch of the pass is enqueued before the GPU reaches it and the events
+        time the GPU work, not the host's launch rate."""
+        C = self.C
+        if hold_cycles > 0:
+            torch.cuda._sleep(int(hold_cycles))
+        ev = []
+        for t, hop in enumerate(self.blocks):
+            row = []
+            for d, blocks in enumerate(hop):
+                if timing:
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                for b in blocks:
+                    kc = b.kv_chunk
+                    s = self.slot[b]
+                    attn_partial(self.q_chunk[b.q_chunk], self.k[:, :, kc * C:(kc + 1) * C],
+                                 self.v[:, :, kc * C:(kc + 1) * C], b.q_chunk * C, kc * C, self.causal,
+                                 self.scale, out=self.o_parts[b.q_chunk][s], lse=self.lse_parts[b.q_chunk][s])
+                if timing:
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e1.record()
+                    row.append((e0, e1))
+            ev.append(row)
+        merge_ev = []
+        for d, dc in enumerate(self.chunks):
+            if timing:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+            for qc in dc:
+                n = self.n_parts[qc]
+                if n == 0:  # no visible key (only without keys at all): O = 0, lse = -inf
+                    self.o[qc].zero_()
+                    self.lse[qc].fill_(-math.inf)
+                    continue
+                lse_merge(self.o_parts[qc][:n], self.lse_parts[qc][:n], torch.bfloat16, out=self.o[qc],
+                          lse=self.lse[qc])
+            if timing:
+                e1 = torch.cuda.Event(enable_timing=True)
+                e1.record()
+                merge_ev.append((e0, e1))
+        if not timing:
+            return None
+        torch.cuda.synchronize()
+        hop_ms = [[a.elapsed_time(b) for a, b in row] for row in ev]
+        merge_ms = [a.elapsed_time(b) for a, b in merge_ev]
+        return hop_ms, merge_ms
+
+    def output(self):
+        o = torch.empty((self.B, self.Hq, self.S, self.D), dtype=torch.bfloat16, device=self.k.device)
+        lse = torch.empty((self.B, self.Hq, self.S), dtype=torch.float32, device=self.k.device)
+        for qc in self.q_chunk:
+            o[:, :, qc * self.C:(qc + 1) * self.C] = self.o[qc]
+            lse[:, :, qc * self.C:(qc + 1) * self.C] = self.lse[qc]
+        return o, lse
+
+
 def ring_attn_fwd_static(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, causal: bool = False,
                          scale: float | None = None, out: torch.Tensor | None = None,
                          lse: torch.Tensor | None = None):

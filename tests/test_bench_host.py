@@ -106,3 +106,10 @@ def test_measured_traffic_follows_the_kernel_sources(tmp_path):
     assert bench.measured_traffic("lse_merge", "wl", str(tmp_path)) == 123
     assert bench.measured_traffic("lse_merge", "other", str(tmp_path)) is None  # stale capture
     assert bench.measured_traffic("attn_partial", "wl", str(tmp_path)) is None
+
+
+def test_ring_time_from_hops():
+    r = bench.ring_time_from_hops([[1.0, 3.0], [2.0, 2.0]])
+    assert r["ring_ms"] == 5.0 and r["device_ms_total"] == 8.0
+    assert r["hop_spread_max_over_mean"] == [1.5, 1.0]
+    assert r["balance"] == 0.8

@@ -199,6 +199,24 @@ def test_lse_merge_part_counts(sa, P, D):
     check_lse(l, lse_ref, tol=1e-5)
 
 
+@pytest.mark.parametrize("layout", ["contiguous", "zigzag"])
+@pytest.mark.parametrize("shape", [(1, 4, 2, 2048, 128, 4), (2, 3, 1, 1536, 64, 3), (1, 2, 2, 1200, 128, 3)],
+                         ids=["gqa_s2048_p4", "d64_s1536_p3", "ragged_chunks_s1200_p3"])
+def test_emulated_ring_layouts_against_oracle(sa, layout, shape):
+    """P emulated ring devices, each computing the blocks the schedule gives it
+    hop by hop (attn_partial at global offsets) and merging per query chunk:
+    the assembled output is the single-pass causal attention."""
+    B, Hq, Hkv, S, D, P = shape
+    q, k, v = workloads.make_qkv(adhoc(B, Hq, Hkv, S, D, True, seed=55))
+    o_ref, lse_ref = oracle.attention(q, k, v, True)
+    ring = sa.EmulatedRing(*to_dev(q, k, v), P=P, layout=layout, causal=True)
+    hop_ms, merge_ms = ring.run(timing=True)
+    assert len(hop_ms) == P and all(len(r) == P for r in hop_ms) and len(merge_ms) == P
+    o, lse = ring.output()
+    check_o(o, o_ref)
+    check_lse(lse, lse_ref)
+
+
 # ----------------------------------------------------------------- full-size workloads
 
 def run_workload(sa, w, q, k, v):

@@ -3,8 +3,10 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
 A step is one pass of the whole path over one batch of the workload: for a
-ring-chunked workload, P attn_partial launches (one per KV chunk, zero-copy
-views) and one lse_merge; for a single-pass workload, one attn_fwd. The
+ring-chunked workload, the P key chunks' partials (by default one
+attn_partial_blocks launch over all P chunks, --partials per-chunk for one
+attn_partial launch per chunk; zero-copy views either way) and one lse_merge;
+for a single-pass workload, one attn_fwd. The
 default workload is the ring-chunked causal attention B=2, H=32, S=4096,
 D=128 with P=8 chunks of 512.
 
@@ -92,6 +94,7 @@ def merge_algorithmic_bytes(w: workloads.Workload, out_bytes: int = 2) -> int:
 
 KERNEL_SOURCES = {
     "attn_partial": ["attn_kernel.cu", "attn_common.cuh", "ptx.cuh"],
+    "attn_partial_blocks": ["attn_kernel.cu", "attn_common.cuh", "ptx.cuh"],
     "attn_fwd": ["attn_kernel.cu", "attn_common.cuh", "ptx.cuh"],
     "lse_merge": ["lse_merge.cu"],
 }
@@ -217,7 +220,9 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int):
     if P > 1:
         o_parts = torch.empty((P, B, Hq, S, D), dtype=torch.float32, device=dev)
         lse_parts = torch.empty((P, B, Hq, S), dtype=torch.float32, device=dev)
-    launches_per_step = P + 1 if P > 1 else 1
+    grouped = P > 1 and args.partials == "grouped"
+    launches_per_step = (2 if grouped else P + 1) if P > 1 else 1
+    chunk_blocks = [(0, j * C, 0, 0, j * C, S, C, j) for j in range(P)]
 
     def step(qq, kk, vv, ev=None):
         if P == 1:
@@ -229,9 +234,13 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int):
             return
         if ev:
             ev[0].record(stream)
-        for j in range(P):
-            sa.attn_partial(qq, kk[:, :, j * C:(j + 1) * C], vv[:, :, j * C:(j + 1) * C], 0, j * C, w.causal,
-                            out=o_parts[j], lse=lse_parts[j], skip_empty=True)
+        if grouped:  # the P chunks' partials in one persistent launch
+            sa.attn_partial_blocks(qq, kk, vv, chunk_blocks, n_parts=P, causal=w.causal, out=o_parts,
+                                   lse=lse_parts, skip_empty=True)
+        else:
+            for j in range(P):
+                sa.attn_partial(qq, kk[:, :, j * C:(j + 1) * C], vv[:, :, j * C:(j + 1) * C], 0, j * C,
+                                w.causal, out=o_parts[j], lse=lse_parts[j], skip_empty=True)
         if ev:
             ev[1].record(stream)
         sa.lse_merge(o_parts, lse_parts, torch.bfloat16, out=o, lse=lse)
@@ -305,14 +314,18 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int):
         del qd, kd, vd
 
     peaks, peak_src = load_peaks()
-    attn_avg_ms = statistics.mean(attn_ms) / (P if P > 1 else 1)  # per launch
-    flops_per_launch = F / (P if P > 1 else 1)
+    n_attn = P if P > 1 and not grouped else 1  # attention launches per step
+    attn_avg_ms = statistics.mean(attn_ms) / n_attn  # per launch
+    flops_per_launch = F / n_attn
     achieved = flops_per_launch / (attn_avg_ms * 1e-3) / 1e12
+    entry = "attn_partial_blocks" if grouped else ("attn_partial" if P > 1 else "attn_fwd")
+    what = {"attn_partial_blocks": f"<f32 out> (attn_partial_blocks: the {P} key chunks in one launch)",
+            "attn_partial": "<f32 out> (attn_partial)", "attn_fwd": "<bf16 out>"}[entry]
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"],
-                "traffic": measured_traffic("attn_partial" if P > 1 else "attn_fwd", w.name),
+                "traffic": measured_traffic(entry, w.name),
                 "kernel": ("attn_fwd_2sm_kernel" if D == 128 and os.environ.get("SEQATTN_ATTN_KERNEL") == "2sm"
-                           else f"attn_fwd_kernel<{D}>") + ("<f32 out> (attn_partial)" if P > 1 else "<bf16 out>"),
+                           and not grouped else f"attn_fwd_kernel<{D}>") + what,
                 "peak_source": f"{peak_src} bf16 burst", "launch_ms": attn_avg_ms}
     merge = None
     if merge_ms:
@@ -419,11 +432,15 @@ def run_ring_schedules(args, w: workloads.Workload) -> dict:
             "speedup_zigzag": out["contiguous"]["ring_ms"] / out["zigzag"]["ring_ms"]}
 
 
-def workload_config(w: workloads.Workload):
-    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "D": w.D, "causal": w.causal,
-            "P": w.P, "chunk": w.chunk, "scale": "1/sqrt(D)",
-            "l2": "no flush: each step writes P fp32 partials and reads them back "
-                  "(>1 GB for ring workloads, inputs >129 MB L2 for single-pass ones)"}
+def workload_config(w: workloads.Workload, partials: str | None = None):
+    c = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "D": w.D, "causal": w.causal,
+         "P": w.P, "chunk": w.chunk, "scale": "1/sqrt(D)",
+         "l2": "no flush: each step writes P fp32 partials and reads them back "
+               "(>1 GB for ring workloads, inputs >129 MB L2 for single-pass ones)"}
+    if w.P > 1 and partials:
+        c["partials"] = ("one attn_partial_blocks launch computes the P key chunks' partials"
+                         if partials == "grouped" else "one attn_partial launch per key chunk")
+    return c
 
 
 def main(argv=None):
@@ -438,6 +455,9 @@ def main(argv=None):
     ap.add_argument("--cpu-baseline-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--partials", default="grouped", choices=["grouped", "per-chunk"],
+                    help="ring workloads: the P chunks' partials in one attn_partial_blocks launch "
+                         "(default) or one attn_partial launch per chunk")
     ap.add_argument("--ring-schedule", action="store_true",
                     help="instead of the step: per-hop device times of the emulated causal ring, "
                          "contiguous vs zigzag layout (ring workloads)")
@@ -481,7 +501,7 @@ def main(argv=None):
         line = {"metric": METRIC, "value": r["value"], "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": workload_config(w), "roofline": r["roofline"], "merge": r["merge"],
+                "config": workload_config(w, args.partials), "roofline": r["roofline"], "merge": r["merge"],
                 "cpu_baseline": cpu, "e2e": r["e2e"], "gpu_launches": r["gpu_launches"], "clocks": r["clocks"]}
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -142,6 +142,67 @@ int attn_debug_expire_wait(unsigned timeout_us, attn_stream_t stream);
  */
 int attn_debug_exp2(const float *x, float *y, long long n, int poly, attn_stream_t stream);
 
+/*
+ * attn_block -- one block of attention over row ranges of packed tensors
+ * (heads outermost, rows contiguous per head, D innermost): the queries in
+ * rows [q_row, q_row + Sq) of every head of Q against the keys and values in
+ * rows [kv_row, kv_row + Skv) of K / V, written to rows [o_row, o_row + Sq) of
+ * part `part` of O and lse. q_pos / kv_pos are the global sequence positions of the block's
+ * query row 0 and key 0: under the causal mask query i sees key j iff
+ * kv_pos + j <= q_pos + i (the masking of page "Ulysses与Ring-Attention序列并行
+ * 技术详解", Ring-Attention part, at global positions; a row that sees no key
+ * gets O = 0, lse = -inf).
+ */
+typedef struct {
+  long long q_row, kv_row, o_row;
+  long long q_pos, kv_pos;
+  int Sq, Skv;
+  int part;
+} attn_block;
+
+/*
+ * attn_partial_blocks -- several attn_partial blocks in one persistent launch
+ * (per 64 blocks): e.g. the blocks one Ring-Attention device computes at one
+ * hop, or every chunk of a ring pass at once.
+ *   q         bf16 [B, Hq, q_rows, D];  k, v  bf16 [B, Hkv, kv_rows, D]
+ *   o_part    fp32 [n_parts, B, Hq, o_rows, D];  lse_part fp32 [n_parts, B, Hq, o_rows]
+ *             (the layout lse_merge reads); block b writes part b.part
+ *   blocks    host array of n_blocks attn_block (read during the call only)
+ *   flags     0 or ATTN_PARTIAL_SKIP_EMPTY (as for attn_partial)
+ * Each block's O rows are normalised within the block (a partial, merged by
+ * lse_merge). Rows of K / V past a block's end, up to the next multiple of
+ * 128, are read and masked: they must hold finite values (they do when they
+ * belong to other blocks or to the same tensor). Blocks must lie inside the
+ * tensors, 0 <= part < n_parts, and the output rows of blocks of the same
+ * part must not overlap, else
+ * ATTN_ERR_INVALID_ARG (as for bad shapes, pointers or alignment); head dims
+ * other than 64 / 128: ATTN_ERR_UNSUPPORTED. Device pointers owned by the
+ * caller; asynchronous on `stream`.
+ */
+int attn_partial_blocks(const void *q, const void *k, const void *v, float *o_part,
+                        float *lse_part, const attn_block *blocks, int n_blocks, int B, int Hq,
+                        int Hkv, long long q_rows, long long kv_rows, long long o_rows,
+                        int n_parts, int D, int causal, float scale, int flags,
+                        attn_stream_t stream);
+
+/*
+ * attn_fwd_varlen -- attention over packed variable-length sequences (the
+ * packing of page "ms-swift集成FlashAttention 2/3，长文本训练更高效": sequences
+ * concatenated without padding, attention kept within each sequence).
+ *   q, o       bf16 [Hq, total_q, D]   (sequence s in rows cu_seqlens_q[s] ..)
+ *   k, v       bf16 [Hkv, total_k, D]  (rows cu_seqlens_k[s] ..)
+ *   lse        fp32 [Hq, total_q]      (natural log)
+ *   cu_seqlens_q / cu_seqlens_k  host int64 arrays of nseq + 1 entries, starting
+ *              at 0, non-decreasing; total_q / total_k are their last entries
+ * Causal masks are aligned at the bottom right of each sequence: query row i
+ * of a sequence sees key j iff j <= i + Skv_s - Sq_s (the usual mask when
+ * Sq_s == Skv_s). Sequences with no query rows are skipped; rows that see no
+ * key get O = 0, lse = -inf. Errors as for attn_partial_blocks.
+ */
+int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                    const long long *cu_seqlens_q, const long long *cu_seqlens_k, int nseq, int Hq,
+                    int Hkv, int D, int causal, float scale, attn_stream_t stream);
+
 /* Size of the library's fixed scratch array used by attn_ring_fwd_static. */
 #define SEQATTN_RING_SCRATCH_BYTES (64ull << 20) /* 64 MiB */
 

@@ -10,6 +10,7 @@ to, and a missing library is an error.
     o_i, lse_i = attn_partial(q, k[:, :, a:b], v[:, :, a:b], q_off=0, kv_off=a, causal=True)
     o, lse = lse_merge(o_parts, lse_parts)
     o, lse = ring_attn_fwd(q, k, v, P=8, causal=True)   # P chunks + merge on one GPU
+    o, lse = attn_fwd_varlen(q, k, v, cu_seqlens, cu_seqlens, causal=True)  # packed sequences
 """
 from __future__ import annotations
 
@@ -17,9 +18,12 @@ import math
 
 import torch
 
-from ._lib import AttnError, lib
+import ctypes
 
-__all__ = ["attn_fwd", "attn_partial", "lse_merge", "ring_attn_fwd", "ring_attn_fwd_static",
+from ._lib import AttnBlock, AttnError, lib
+
+__all__ = ["attn_fwd", "attn_partial", "attn_partial_blocks", "attn_fwd_varlen", "lse_merge",
+           "ring_attn_fwd", "ring_attn_fwd_static", "EmulatedRing",
            "query_device_error", "AttnError", "lib", "RING_SCRATCH_BYTES"]
 
 RING_SCRATCH_BYTES = 64 << 20  # the library's fixed scratch array for ring_attn_fwd_static
@@ -113,6 +117,77 @@ def attn_partial(q: torch.Tensor, k_chunk: torch.Tensor, v_chunk: torch.Tensor, 
     return out, lse
 
 
+def attn_partial_blocks(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, blocks, n_parts: int = 1,
+                        o_rows: int | None = None, causal: bool = False, scale: float | None = None,
+                        out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                        skip_empty: bool = False):
+    """Several attention blocks in one persistent launch (per 64 blocks).
+
+    q bf16 [B,Hq,q_rows,D], k/v bf16 [B,Hkv,kv_rows,D], contiguous; blocks: an
+    iterable of (q_row, kv_row, o_row, q_pos, kv_pos, Sq, Skv, part) with the
+    meaning of attn_block in include/seqattn.h. Returns the partials (O fp32
+    [n_parts,B,Hq,o_rows,D], lse fp32 [n_parts,B,Hq,o_rows]); rows no block
+    writes keep their previous contents (uninitialised unless out/lse are given)."""
+    _require(q.dim() == 4 and k.dim() == 4 and v.shape == k.shape, "expected [B,H,S,D] tensors")
+    B, Hq, q_rows, D = q.shape
+    Hkv, kv_rows = k.shape[1], k.shape[2]
+    for t in (q, k, v):
+        _require(t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous(),
+                 "q, k, v must be contiguous bf16 CUDA tensors")
+    blocks = list(blocks)
+    o_rows = q_rows if o_rows is None else int(o_rows)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty((n_parts, B, Hq, o_rows, D), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((n_parts, B, Hq, o_rows), dtype=torch.float32, device=q.device)
+    _require(out.shape == (n_parts, B, Hq, o_rows, D) and out.dtype == torch.float32 and out.is_contiguous(),
+             "bad out")
+    _require(lse.shape == (n_parts, B, Hq, o_rows) and lse.dtype == torch.float32 and lse.is_contiguous(),
+             "bad lse")
+    arr = (AttnBlock * max(len(blocks), 1))(*[AttnBlock(*map(int, b)) for b in blocks])
+    st = lib.attn_partial_blocks(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                 ctypes.addressof(arr), len(blocks), B, Hq, Hkv, q_rows, kv_rows, o_rows,
+                                 int(n_parts), D, int(bool(causal)), scale,
+                                 ATTN_PARTIAL_SKIP_EMPTY if skip_empty else 0, _stream_handle(q.device))
+    _check(st, "attn_partial_blocks")
+    return out, lse
+
+
+def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q, cu_seqlens_k,
+                    causal: bool = False, scale: float | None = None, out: torch.Tensor | None = None,
+                    lse: torch.Tensor | None = None):
+    """Attention over packed variable-length sequences: q bf16 [Hq,total_q,D],
+    k/v bf16 [Hkv,total_k,D] (sequence s in rows cu_seqlens[s]..cu_seqlens[s+1]);
+    cu_seqlens_* are host sequences of ints (nseq + 1 entries, from 0). Causal
+    masks are aligned at the bottom right of each sequence. Returns (O bf16
+    [Hq,total_q,D], lse fp32 [Hq,total_q])."""
+    _require(q.dim() == 3 and k.dim() == 3 and v.shape == k.shape, "expected [H,total,D] tensors")
+    Hq, total_q, D = q.shape
+    Hkv, total_k = k.shape[0], k.shape[1]
+    for t in (q, k, v):
+        _require(t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous(),
+                 "q, k, v must be contiguous bf16 CUDA tensors")
+    cq = [int(x) for x in cu_seqlens_q]
+    ck = [int(x) for x in cu_seqlens_k]
+    _require(len(cq) == len(ck) and len(cq) >= 1, "cu_seqlens_q and cu_seqlens_k need nseq + 1 entries")
+    _require(cq[-1] == total_q and ck[-1] == total_k, "cu_seqlens must end at the packed lengths")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
+    _require(out.shape == q.shape and out.dtype == torch.bfloat16 and out.is_contiguous(), "bad out")
+    _require(lse.shape == (Hq, total_q) and lse.dtype == torch.float32 and lse.is_contiguous(), "bad lse")
+    aq = (ctypes.c_longlong * len(cq))(*cq)
+    ak = (ctypes.c_longlong * len(ck))(*ck)
+    st = lib.attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                             ctypes.addressof(aq), ctypes.addressof(ak), len(cq) - 1, Hq, Hkv, D,
+                             int(bool(causal)), scale, _stream_handle(q.device))
+    _check(st, "attn_fwd_varlen")
+    return out, lse
+
+
 def lse_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, out_dtype=torch.bfloat16,
               out: torch.Tensor | None = None, lse: torch.Tensor | None = None):
     """Merge P partials: o_parts fp32 [P,B,H,S,D], lse_parts fp32 [P,B,H,S] -> (O, lse)."""
@@ -137,12 +212,14 @@ def lse_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, out_dtype=torch.bf
 def ring_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, causal: bool = False,
                   scale: float | None = None, o_parts: torch.Tensor | None = None,
                   lse_parts: torch.Tensor | None = None, out: torch.Tensor | None = None,
-                  lse: torch.Tensor | None = None):
+                  lse: torch.Tensor | None = None, grouped: bool = False):
     """Ring-Attention's per-device arithmetic on one GPU: the keys are split into
     P equal chunks (S % P == 0); chunk j is attended by attn_partial at kv_off =
     j*S/P (a zero-copy view), then the P partials are merged by lse_merge. Rows a
     chunk cannot see are not written in o_parts (their lse is -inf).
-    o_parts / lse_parts are optional preallocated fp32 [P,B,Hq,S,D] / [P,B,Hq,S]."""
+    o_parts / lse_parts are optional preallocated fp32 [P,B,Hq,S,D] / [P,B,Hq,S].
+    grouped: the P partials in one attn_partial_blocks launch instead of P
+    attn_partial launches (same results)."""
     B, Hq, S, D = q.shape
     _require(P >= 1 and S % P == 0, "S must be a multiple of P")
     C = S // P
@@ -150,55 +227,81 @@ def ring_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, cau
         o_parts = torch.empty((P, B, Hq, S, D), dtype=torch.float32, device=q.device)
     if lse_parts is None:
         lse_parts = torch.empty((P, B, Hq, S), dtype=torch.float32, device=q.device)
-    for j in range(P):
-        attn_partial(q, k[:, :, j * C:(j + 1) * C], v[:, :, j * C:(j + 1) * C], 0, j * C, causal, scale,
-                     out=o_parts[j], lse=lse_parts[j], skip_empty=True)
+    if grouped:
+        attn_partial_blocks(q, k, v, [(0, j * C, 0, 0, j * C, S, C, j) for j in range(P)], n_parts=P,
+                            causal=causal, scale=scale, out=o_parts, lse=lse_parts, skip_empty=True)
+    else:
+        for j in range(P):
+            attn_partial(q, k[:, :, j * C:(j + 1) * C], v[:, :, j * C:(j + 1) * C], 0, j * C, causal, scale,
+                         out=o_parts[j], lse=lse_parts[j], skip_empty=True)
     return lse_merge(o_parts, lse_parts, torch.bfloat16, out=out, lse=lse)
 
 
 class EmulatedRing:
-    """P ring devices emulated on one GPU, each with its own chunks of Q (copied
-    to device-local contiguous buffers, as each device would hold its shard) and
-    its own fp32 partials. K/V chunks are read in place (a "hop" moves no bytes
-    on one GPU). The blocks each device computes at each hop follow
-    ``ring_schedule.hop_blocks`` for the layout ("contiguous": the pages' ring,
-    one chunk per device; "zigzag": chunks d and 2P-1-d, balanced under the
-    causal mask).
+    """P ring devices emulated on one GPU. The blocks each device computes at
+    each hop follow ``ring_schedule.hop_blocks`` for the layout ("contiguous":
+    the pages' ring, one chunk per device; "zigzag": chunks d and 2P-1-d,
+    balanced under the causal mask). K/V chunks are read in place (a "hop"
+    moves no bytes on one GPU); each block's fp32 partial has its own slot,
+    the slots of a query chunk adjacent, so that chunk's merge reads them as
+    one [n, B, Hq, C, D] stack.
 
-    run() launches, hop by hop and device by device, one attn_partial per block
-    (the query chunk's rows against the key chunk, global offsets for the
-    mask), then per query chunk one lse_merge of its partials; with timing, the
-    launches of each (hop, device) are bracketed by CUDA events. output()
-    assembles the devices' results into [B,Hq,S,D] / [B,Hq,S] (test glue)."""
+    run() launches, hop by hop and device by device, the device's blocks --
+    one attn_partial_blocks launch per (hop, device) when fused, else one
+    attn_partial per block (device-local contiguous Q chunk) -- then per query
+    chunk one lse_merge of its partials; with timing, the launches of each
+    (hop, device) are bracketed by CUDA events. output() assembles the
+    devices' results into [B,Hq,S,D] / [B,Hq,S] (test glue)."""
 
     def __init__(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, layout: str = "zigzag",
-                 causal: bool = True, scale: float | None = None):
+                 causal: bool = True, scale: float | None = None, fused: bool = True):
         from . import ring_schedule as rs
 
         B, Hq, S, D = q.shape
         nc = rs.n_chunks(P, layout)
         _require(S % nc == 0, f"S must be a multiple of {nc} for the {layout} layout with P = {P}")
+        _require(q.is_contiguous() and k.is_contiguous() and v.is_contiguous(), "q, k, v must be contiguous")
         self.B, self.Hq, self.S, self.D, self.P, self.layout = B, Hq, S, D, P, layout
-        self.causal, self.scale, self.k, self.v = causal, scale, k, v
-        self.C = S // nc
+        self.causal, self.scale, self.fused = causal, scale, fused
+        self.q, self.k, self.v = q, k, v
+        self.C = C = S // nc
         self.chunks = rs.device_chunks(P, layout)
         self.blocks = rs.hop_blocks(P, layout, causal)
-        C = self.C
-        self.q_chunk = {qc: q[:, :, qc * C:(qc + 1) * C].contiguous() for dc in self.chunks for qc in dc}
-        # partial slot of each block within its query chunk's stack, in hop order
-        self.slot, n_parts = {}, {qc: 0 for qc in self.q_chunk}
+        qcs = [qc for dc in self.chunks for qc in dc]
+        n_parts = {qc: 0 for qc in qcs}
+        slot = {}
         for hop in self.blocks:
             for blocks in hop:
                 for b in blocks:
-                    self.slot[b] = n_parts[b.q_chunk]
+                    slot[b] = n_parts[b.q_chunk]
                     n_parts[b.q_chunk] += 1
-        self.o_parts = {qc: torch.empty((max(n, 1), B, Hq, C, D), dtype=torch.float32, device=q.device)
-                        for qc, n in n_parts.items()}
-        self.lse_parts = {qc: torch.empty((max(n, 1), B, Hq, C), dtype=torch.float32, device=q.device)
-                          for qc, n in n_parts.items()}
-        self.n_parts = n_parts
-        self.o = {qc: torch.empty((B, Hq, C, D), dtype=torch.bfloat16, device=q.device) for qc in self.q_chunk}
-        self.lse = {qc: torch.empty((B, Hq, C), dtype=torch.float32, device=q.device) for qc in self.q_chunk}
+        first, total = {}, 0
+        for qc in sorted(qcs):
+            first[qc] = total
+            total += n_parts[qc]
+        self.n_parts, self.first = n_parts, first
+        self.part = {b: first[b.q_chunk] + s for b, s in slot.items()}
+        self.o_all = torch.empty((max(total, 1), B, Hq, C, D), dtype=torch.float32, device=q.device)
+        self.lse_all = torch.empty((max(total, 1), B, Hq, C), dtype=torch.float32, device=q.device)
+        self.q_chunk = {} if fused else {qc: q[:, :, qc * C:(qc + 1) * C].contiguous() for qc in qcs}
+        self.o = {qc: torch.empty((B, Hq, C, D), dtype=torch.bfloat16, device=q.device) for qc in qcs}
+        self.lse = {qc: torch.empty((B, Hq, C), dtype=torch.float32, device=q.device) for qc in qcs}
+
+    def _launch_device_hop(self, blocks):
+        C = self.C
+        if self.fused:
+            if blocks:
+                attn_partial_blocks(self.q, self.k, self.v,
+                                    [(b.q_chunk * C, b.kv_chunk * C, 0, b.q_chunk * C, b.kv_chunk * C, C, C,
+                                      self.part[b]) for b in blocks],
+                                    n_parts=self.o_all.shape[0], o_rows=C, causal=self.causal,
+                                    scale=self.scale, out=self.o_all, lse=self.lse_all)
+            return
+        for b in blocks:
+            kc, s = b.kv_chunk, self.part[b]
+            attn_partial(self.q_chunk[b.q_chunk], self.k[:, :, kc * C:(kc + 1) * C],
+                         self.v[:, :, kc * C:(kc + 1) * C], b.q_chunk * C, kc * C, self.causal, self.scale,
+                         out=self.o_all[s], lse=self.lse_all[s])
 
     def run(self, timing: bool = False, hold_cycles: int = 0):
         """One ring pass. With timing, returns ms[t][d] (the launches of device
@@ -206,39 +309,33 @@ class EmulatedRing:
         > 0 first queues a GPU-side wait of that many clocks, so that every
         launch of the pass is enqueued before the GPU reaches it and the events
         time the GPU work, not the host's launch rate."""
-        C = self.C
         if hold_cycles > 0:
             torch.cuda._sleep(int(hold_cycles))
         ev = []
-        for t, hop in enumerate(self.blocks):
+        for hop in self.blocks:
             row = []
-            for d, blocks in enumerate(hop):
+            for blocks in hop:
                 if timing:
                     e0 = torch.cuda.Event(enable_timing=True)
                     e0.record()
-                for b in blocks:
-                    kc = b.kv_chunk
-                    s = self.slot[b]
-                    attn_partial(self.q_chunk[b.q_chunk], self.k[:, :, kc * C:(kc + 1) * C],
-                                 self.v[:, :, kc * C:(kc + 1) * C], b.q_chunk * C, kc * C, self.causal,
-                                 self.scale, out=self.o_parts[b.q_chunk][s], lse=self.lse_parts[b.q_chunk][s])
+                self._launch_device_hop(blocks)
                 if timing:
                     e1 = torch.cuda.Event(enable_timing=True)
                     e1.record()
                     row.append((e0, e1))
             ev.append(row)
         merge_ev = []
-        for d, dc in enumerate(self.chunks):
+        for dc in self.chunks:
             if timing:
                 e0 = torch.cuda.Event(enable_timing=True)
                 e0.record()
             for qc in dc:
-                n = self.n_parts[qc]
+                n, f = self.n_parts[qc], self.first[qc]
                 if n == 0:  # no visible key (only without keys at all): O = 0, lse = -inf
                     self.o[qc].zero_()
                     self.lse[qc].fill_(-math.inf)
                     continue
-                lse_merge(self.o_parts[qc][:n], self.lse_parts[qc][:n], torch.bfloat16, out=self.o[qc],
+                lse_merge(self.o_all[f:f + n], self.lse_all[f:f + n], torch.bfloat16, out=self.o[qc],
                           lse=self.lse[qc])
             if timing:
                 e1 = torch.cuda.Event(enable_timing=True)
@@ -254,7 +351,7 @@ class EmulatedRing:
     def output(self):
         o = torch.empty((self.B, self.Hq, self.S, self.D), dtype=torch.bfloat16, device=self.k.device)
         lse = torch.empty((self.B, self.Hq, self.S), dtype=torch.float32, device=self.k.device)
-        for qc in self.q_chunk:
+        for qc in self.o:
             o[:, :, qc * self.C:(qc + 1) * self.C] = self.o[qc]
             lse[:, :, qc * self.C:(qc + 1) * self.C] = self.lse[qc]
         return o, lse

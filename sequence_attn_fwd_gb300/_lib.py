@@ -14,10 +14,17 @@ LIB_PATH = os.path.join(_PKG, "lib", "libseqattn.so")
 # Every function the public header include/seqattn.h declares.
 EXPORTS = ["attn_fwd", "attn_partial", "lse_merge", "attn_query_device_error",
            "attn_status_string", "attn_last_cuda_error", "attn_ring_fwd_static",
-           "attn_debug_expire_wait", "attn_debug_exp2"]
+           "attn_debug_expire_wait", "attn_debug_exp2", "attn_partial_blocks", "attn_fwd_varlen"]
 
 STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
           3: "ATTN_ERR_CUDA", 4: "ATTN_ERR_TIMEOUT"}
+
+
+class AttnBlock(ctypes.Structure):
+    """attn_block of include/seqattn.h."""
+    _fields_ = [("q_row", ctypes.c_longlong), ("kv_row", ctypes.c_longlong), ("o_row", ctypes.c_longlong),
+                ("q_pos", ctypes.c_longlong), ("kv_pos", ctypes.c_longlong), ("Sq", ctypes.c_int),
+                ("Skv", ctypes.c_int), ("part", ctypes.c_int)]
 
 
 class AttnError(RuntimeError):
@@ -47,6 +54,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.attn_debug_expire_wait.restype = ctypes.c_int
     L.attn_debug_exp2.argtypes = [P, P, ctypes.c_longlong, ctypes.c_int, P]
     L.attn_debug_exp2.restype = ctypes.c_int
+    L.attn_partial_blocks.argtypes = [P, P, P, P, P, P, I, I, I, I, LL, LL, LL, I, I, I, F, I, P]
+    L.attn_partial_blocks.restype = ctypes.c_int
+    L.attn_fwd_varlen.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, F, P]
+    L.attn_fwd_varlen.restype = ctypes.c_int
     for name in ("attn_fwd", "attn_partial", "lse_merge", "attn_query_device_error",
                  "attn_last_cuda_error"):
         getattr(L, name).restype = ctypes.c_int

@@ -7,8 +7,10 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "../../include/seqattn.h"
 #include "kernels.h"
@@ -128,13 +130,143 @@ int run_attention(const void *q, const void *k, const void *v, long long q_off, 
   p.causal = causal;
   p.n_qblocks = (Sq + 255) / 256;
   p.skip_empty = skip_empty ? 1 : 0;
+  p.o_rows = Sq;
   cudaError_t e = seqattn::launch_attention(D, f32_out, pair, tq, tk, tv, to, p, stream);
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+// Attention over a list of blocks (row ranges of packed [heads][rows][D]
+// tensors), launched in tables of at most kMaxLaunchBlocks blocks. The caller
+// has validated shapes, pointers and ranges.
+int run_blocks(const void *q, const void *k, const void *v, void *o, float *lse,
+               const std::vector<seqattn::BlockDesc> &blocks, int B, int Hq, int Hkv,
+               long long q_rows, long long kv_rows, long long o_rows, int n_parts, int D,
+               int causal, float scale, bool f32_out, bool skip_empty, cudaStream_t stream) {
+  if (blocks.empty() || B == 0) return ATTN_OK;
+  CUtensorMap tq, tk, tv, to;
+  const long long heads = static_cast<long long>(B) * Hq, kv_heads = static_cast<long long>(B) * Hkv;
+  const long long o_heads = heads * n_parts;
+  if (!make_map(&tq, q, D, q_rows > 0 ? q_rows : 1, heads, (q_rows > 0 ? q_rows : 1) * D) ||
+      !make_map(&tk, k, D, kv_rows > 0 ? kv_rows : 1, kv_heads, (kv_rows > 0 ? kv_rows : 1) * D) ||
+      !make_map(&tv, v, D, kv_rows > 0 ? kv_rows : 1, kv_heads, (kv_rows > 0 ? kv_rows : 1) * D) ||
+      !make_out_map(&to, o, D, o_rows > 0 ? o_rows : 1, o_heads, f32_out))
+    return cuda_fail(cudaErrorInvalidValue);
+  seqattn::AttnParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.causal = causal;
+  p.skip_empty = skip_empty ? 1 : 0;
+  p.o_rows = o_rows;
+  for (size_t first = 0; first < blocks.size(); first += seqattn::kMaxLaunchBlocks) {
+    seqattn::BlockTable tbl{};
+    const size_t n = std::min(blocks.size() - first, static_cast<size_t>(seqattn::kMaxLaunchBlocks));
+    tbl.n = static_cast<int>(n);
+    long long items = 0;
+    for (size_t i = 0; i < n; ++i) {
+      tbl.b[i] = blocks[first + i];
+      tbl.item_start[i] = items;
+      items += heads * ((blocks[first + i].Sq + 255) / 256);
+    }
+    tbl.item_start[n] = items;
+    cudaError_t e = seqattn::launch_attention_blocks(D, f32_out, tq, tk, tv, to, p, tbl, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return ATTN_OK;
+}
+
+// Checks shared by the block entry points; blocks must lie inside the tensors
+// and the output rows of blocks of the same part must not overlap.
+int check_blocks(const std::vector<seqattn::BlockDesc> &blocks, long long q_rows, long long kv_rows,
+                 long long o_rows, int n_parts) {
+  if (q_rows < 0 || kv_rows < 0 || o_rows < 0 || q_rows > kMaxRowsPerHead ||
+      kv_rows > kMaxRowsPerHead || o_rows > kMaxRowsPerHead || n_parts < 1)
+    return ATTN_ERR_INVALID_ARG;
+  std::vector<std::pair<std::pair<int, long long>, long long>> outs;
+  for (const auto &b : blocks) {
+    if (b.Sq < 0 || b.Skv < 0 || b.q_row < 0 || b.kv_row < 0 || b.o_row < 0) return ATTN_ERR_INVALID_ARG;
+    if (b.part < 0 || b.part >= n_parts) return ATTN_ERR_INVALID_ARG;
+    if (b.q_row + b.Sq > q_rows || b.kv_row + b.Skv > kv_rows || b.o_row + b.Sq > o_rows)
+      return ATTN_ERR_INVALID_ARG;
+    if (b.q_pos < -kMaxRowsPerHead * 4 || b.q_pos > kMaxRowsPerHead * 4 ||
+        b.kv_pos < -kMaxRowsPerHead * 4 || b.kv_pos > kMaxRowsPerHead * 4)
+      return ATTN_ERR_INVALID_ARG;
+    if (b.Sq > 0) outs.push_back({{b.part, b.o_row}, b.o_row + b.Sq});
+  }
+  std::sort(outs.begin(), outs.end());
+  for (size_t i = 1; i < outs.size(); ++i)
+    if (outs[i].first.first == outs[i - 1].first.first && outs[i].first.second < outs[i - 1].second)
+      return ATTN_ERR_INVALID_ARG;  // overlapping outputs
+  return ATTN_OK;
+}
+
+int check_common(const void *q, const void *k, const void *v, const void *o, const float *lse, int B,
+                 int Hq, int Hkv, int D, int causal, float scale) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (!scale_ok(scale)) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Hq > 0x7fffffffll) return ATTN_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
 }
 
 }  // namespace
 
 extern "C" {
+
+int attn_partial_blocks(const void *q, const void *k, const void *v, float *o_part, float *lse_part,
+                        const attn_block *blocks, int n_blocks, int B, int Hq, int Hkv,
+                        long long q_rows, long long kv_rows, long long o_rows, int n_parts, int D,
+                        int causal, float scale, int flags, attn_stream_t stream) {
+  if (flags & ~ATTN_PARTIAL_SKIP_EMPTY) return ATTN_ERR_INVALID_ARG;
+  if (n_blocks < 0 || (n_blocks > 0 && !blocks)) return ATTN_ERR_INVALID_ARG;
+  if (n_blocks == 0 || B == 0) return (B < 0) ? ATTN_ERR_INVALID_ARG : ATTN_OK;
+  int st = check_common(q, k, v, o_part, lse_part, B, Hq, Hkv, D, causal, scale);
+  if (st != ATTN_OK) return st;
+  std::vector<seqattn::BlockDesc> bl(static_cast<size_t>(n_blocks));
+  for (int i = 0; i < n_blocks; ++i)
+    bl[i] = {blocks[i].q_row, blocks[i].kv_row, blocks[i].o_row, blocks[i].q_pos, blocks[i].kv_pos,
+             blocks[i].Sq, blocks[i].Skv, blocks[i].part};
+  st = check_blocks(bl, q_rows, kv_rows, o_rows, n_parts);
+  if (st != ATTN_OK) return st;
+  if (static_cast<long long>(B) * Hq * n_parts > 0x7fffffffll) return ATTN_ERR_UNSUPPORTED;
+  return run_blocks(q, k, v, o_part, lse_part, bl, B, Hq, Hkv, q_rows, kv_rows, o_rows, n_parts, D,
+                    causal, scale, true, (flags & ATTN_PARTIAL_SKIP_EMPTY) != 0,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                    const long long *cu_seqlens_q, const long long *cu_seqlens_k, int nseq, int Hq,
+                    int Hkv, int D, int causal, float scale, attn_stream_t stream) {
+  if (nseq < 0 || (nseq > 0 && (!cu_seqlens_q || !cu_seqlens_k))) return ATTN_ERR_INVALID_ARG;
+  if (nseq == 0) return ATTN_OK;
+  if (cu_seqlens_q[0] != 0 || cu_seqlens_k[0] != 0) return ATTN_ERR_INVALID_ARG;
+  std::vector<seqattn::BlockDesc> bl(static_cast<size_t>(nseq));
+  for (int s = 0; s < nseq; ++s) {
+    const long long sq = cu_seqlens_q[s + 1] - cu_seqlens_q[s];
+    const long long sk = cu_seqlens_k[s + 1] - cu_seqlens_k[s];
+    if (sq < 0 || sk < 0 || sq > kMaxRowsPerHead || sk > kMaxRowsPerHead) return ATTN_ERR_INVALID_ARG;
+    // causal: aligned at the bottom right (query row i of a sequence sees keys j <= i + sk - sq)
+    bl[s] = {cu_seqlens_q[s], cu_seqlens_k[s], cu_seqlens_q[s], sk - sq, 0, static_cast<int>(sq),
+             static_cast<int>(sk), 0};
+  }
+  const long long total_q = cu_seqlens_q[nseq], total_k = cu_seqlens_k[nseq];
+  if (total_q == 0) return ATTN_OK;
+  int st = check_common(q, k, v, o, lse, 1, Hq, Hkv, D, causal, scale);
+  if (st != ATTN_OK) return st;
+  st = check_blocks(bl, total_q, total_k, total_q, 1);
+  if (st != ATTN_OK) return st;
+  return run_blocks(q, k, v, o, lse, bl, 1, Hq, Hkv, total_q, total_k, total_q, 1, D, causal, scale,
+                    false, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
 
 int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
              int Hkv, int S, int D, int causal, float scale, attn_stream_t stream) {

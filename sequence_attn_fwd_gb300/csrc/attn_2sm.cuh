@@ -92,7 +92,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int r = 0; r < kRowsPerCluster; r += kRowsPerTile) any = any || kv_tiles_for(p, row0 + r) > 0;
     if (!any) {
       for (int g = 0; g < 2; ++g)
-        write_empty_rows<kD, kF32Out>(p, bh, row0 + 256 * g + kRowsPerTile * static_cast<int>(rank),
+        write_empty_rows<kD, kF32Out>(p, whole_problem(p), bh,
+                                      row0 + 256 * g + kRowsPerTile * static_cast<int>(rank),
                                       kRowsPerTile, threadIdx.x, blockDim.x);
       return;
     }
@@ -252,9 +253,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t pfull_local = bar(kBarPFull + g);
     const uint32_t pfull_leader = mapa_shared(pfull_local, 0);
-    softmax_row<kD, kF32Out>(p, row, tile_first, g ? n_grp[1] : n_grp[0], tS(g) + lane_off,
-                             tO(g) + lane_off, bar(kBarSFull + g), bar(kBarOFull + g), 0, 0u,
-                             static_cast<size_t>(bh) * p.Sq + row, abort_flag, err,
+    softmax_row<kD, kF32Out>(p, whole_problem(p), row, tile_first, g ? n_grp[1] : n_grp[0],
+                             tS(g) + lane_off, tO(g) + lane_off, bar(kBarSFull + g),
+                             bar(kBarOFull + g), 0, 0u, static_cast<size_t>(bh) * p.o_rows + row,
+                             abort_flag, err,
                              EpilogueStore{nullptr, 0u, 0, 0}, [&] {
                                __syncwarp();
                                if (lane == 0) {

@@ -16,17 +16,26 @@ constexpr int kColBlockBytes = 128 * 128;  // 128 rows x 128 bytes (64 bf16) swi
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows > 2^8
 
+// The whole of a single problem as one block.
+__host__ __device__ __forceinline__ BlockDesc whole_problem(const AttnParams &p) {
+  return {0, 0, 0, p.q_off, p.kv_off, p.Sq, p.Skv, 0};
+}
+
 // Per-tile number of KV tiles to visit (0 when the tile has no valid row or
-// none of its rows sees any key).
-__device__ __forceinline__ int kv_tiles_for(const AttnParams &p, int first_row) {
-  const int n_all = (p.Skv + kRowsPerTile - 1) / kRowsPerTile;
-  if (first_row >= p.Sq || n_all == 0) return 0;
-  if (!p.causal) return n_all;
-  const int last_row = min(first_row + kRowsPerTile - 1, p.Sq - 1);
-  const long long max_key = p.q_off + last_row - p.kv_off;  // largest visible key index
+// none of its rows sees any key); first_row is the tile's first row within
+// the block.
+__device__ __forceinline__ int kv_tiles_for(const BlockDesc &b, int causal, int first_row) {
+  const int n_all = (b.Skv + kRowsPerTile - 1) / kRowsPerTile;
+  if (first_row >= b.Sq || n_all == 0) return 0;
+  if (!causal) return n_all;
+  const int last_row = min(first_row + kRowsPerTile - 1, b.Sq - 1);
+  const long long max_key = b.q_pos + last_row - b.kv_pos;  // largest visible key index
   if (max_key < 0) return 0;
   const long long n = max_key / kRowsPerTile + 1;
   return n < n_all ? static_cast<int>(n) : n_all;
+}
+__device__ __forceinline__ int kv_tiles_for(const AttnParams &p, int first_row) {
+  return kv_tiles_for(whole_problem(p), p.causal, first_row);
 }
 
 // Maximum of the 128 scores of a row (raw, before scaling).
@@ -133,11 +142,11 @@ __device__ __forceinline__ float exp_row(const float *s, float c2, float m_ref, 
 // memory, so the zero fill is one coalesced run of 16-byte stores by the
 // `nthreads` threads taking part (tid = 0 .. nthreads - 1).
 template <int D, bool kF32Out>
-__device__ __forceinline__ void write_empty_rows(const AttnParams &p, int bh, int row_begin,
-                                                 int nrows, int tid, int nthreads) {
-  const int rows = min(nrows, p.Sq - row_begin);
+__device__ __forceinline__ void write_empty_rows(const AttnParams &p, const BlockDesc &blk, int bh,
+                                                 int row_begin, int nrows, int tid, int nthreads) {
+  const int rows = min(nrows, blk.Sq - row_begin);
   if (rows <= 0) return;
-  const size_t base = static_cast<size_t>(bh) * p.Sq + row_begin;
+  const size_t base = static_cast<size_t>(bh) * p.o_rows + blk.o_row + row_begin;
   for (int i = tid; i < rows; i += nthreads) p.lse[base + i] = -INFINITY;
   if (p.skip_empty) return;
   const size_t n16 = static_cast<size_t>(rows) * D * (kF32Out ? 4 : 2) / 16;
@@ -170,14 +179,15 @@ struct EpilogueStore {
 //   ofull_parity      parity of the bar_ofull phase that marks this tile's O
 // Returns false if the pipeline was aborted.
 template <int D, bool kF32Out, typename SignalP>
-__device__ __forceinline__ bool softmax_row(const AttnParams &p, int row, int tile_first_row, int n,
+__device__ __forceinline__ bool softmax_row(const AttnParams &p, const BlockDesc &blk, int row,
+                                            int tile_first_row, int n,
                                             uint32_t s_addr, uint32_t o_addr, uint32_t bar_sfull,
                                             uint32_t bar_ofull, int step_base,
                                             uint32_t ofull_parity, size_t row_index,
                                             volatile int *abort_flag, int *err,
                                             const EpilogueStore &store, SignalP signal_p) {
-    const long long qpos = p.q_off + row;
-    const long long tile_first_q = p.q_off + tile_first_row;
+    const long long qpos = blk.q_pos + row;
+    const long long tile_first_q = blk.q_pos + tile_first_row;
     const float c2 = p.scale_log2;
     float m = -INFINITY;  // running max of scale*log2(e)*s (the reference for P)
     float l = 0.f;        // running sum of P relative to m
@@ -190,13 +200,13 @@ __device__ __forceinline__ bool softmax_row(const AttnParams &p, int row, int ti
       if (!ok) break;
       tc_fence_after();
       const int kv0 = j * kRowsPerTile;
-      const bool tail = kv0 + kRowsPerTile > p.Skv;
-      const bool diag = p.causal && (p.kv_off + kv0 + kRowsPerTile - 1 > tile_first_q);
+      const bool tail = kv0 + kRowsPerTile > blk.Skv;
+      const bool diag = p.causal && (blk.kv_pos + kv0 + kRowsPerTile - 1 > tile_first_q);
       int last = 127;  // last visible column of this row in the tile
       if (tail || diag) {
-        long long lim = static_cast<long long>(p.Skv) - kv0 - 1;
+        long long lim = static_cast<long long>(blk.Skv) - kv0 - 1;
         if (p.causal) {
-          const long long c_lim = qpos - p.kv_off - kv0;
+          const long long c_lim = qpos - blk.kv_pos - kv0;
           lim = c_lim < lim ? c_lim : lim;
         }
         last = static_cast<int>(lim < -1 ? -1 : (lim > 127 ? 127 : lim));
@@ -272,16 +282,19 @@ __device__ __forceinline__ bool softmax_row(const AttnParams &p, int row, int ti
       have_o = __all_sync(0xffffffffu, mbar_wait(bar_ofull, ofull_parity, abort_flag, err));
       tc_fence_after();
     }
-    const bool row_valid = row < p.Sq;
+    const bool row_valid = row < blk.Sq;
     const bool write_o = row_valid && !(p.skip_empty && l == 0.f);
     const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
     bool via_tma = store.map != nullptr;
     if (via_tma) {
       // Whole-box stores need the final O on every row, no row that must stay
-      // unwritten (skip_empty rows before the chunk's first key) and a first
-      // row inside the tensor.
-      const bool keep_rows = p.skip_empty && p.causal && (p.q_off + tile_first_row < p.kv_off);
-      via_tma = named_bar_and(store.named_bar, 128, have_o) && !keep_rows && tile_first_row < p.Sq;
+      // unwritten (skip_empty rows before the chunk's first key), and a box
+      // that ends inside the block or at the end of the tensor (the map clips
+      // there; elsewhere the box would spill into the next block's rows).
+      const bool keep_rows = p.skip_empty && p.causal && (blk.q_pos + tile_first_row < blk.kv_pos);
+      const bool box_fits = tile_first_row < blk.Sq &&
+                            (tile_first_row + kRowsPerTile <= blk.Sq || blk.o_row + blk.Sq == p.o_rows);
+      via_tma = named_bar_and(store.named_bar, 128, have_o) && !keep_rows && box_fits;
     }
     if (via_tma) {
       constexpr int kChunkCols = kF32Out ? 32 : 64;  // 128 bytes of a row
@@ -327,7 +340,8 @@ __device__ __forceinline__ bool softmax_row(const AttnParams &p, int row, int ti
         __syncwarp();
         named_bar_sync(store.named_bar, 128);
         if (leader) {
-          tma_store_3d(store.map, buf, c * kChunkCols, tile_first_row, store.head);
+          tma_store_3d(store.map, buf, c * kChunkCols, static_cast<int>(blk.o_row + tile_first_row),
+                       store.head);
           bulk_commit_group();
         }
       }

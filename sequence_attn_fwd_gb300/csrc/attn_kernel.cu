@@ -67,12 +67,13 @@ struct Cfg {
 static_assert(Cfg<128>::kSmemBytes <= 232448 && Cfg<64>::kSmemBytes <= 232448,
               "shared memory per CTA");
 
-// Work item k of a launch: a block of 256 query rows of one (batch, head).
-// Items are numbered with the head fastest; causal launches number the longest
-// query blocks (most KV tiles) first.
+// Work item k of a launch: 256 query rows of one (batch, head) of one block of
+// the launch's table. Within a block, items are numbered with the head
+// fastest; causal launches number the longest query rows (most KV tiles) first.
 struct Item {
+  int blk;   // block of the table
   int bh;    // b * Hq + hq
-  int row0;  // first query row of the block
+  int row0;  // first query row within the block
 };
 // The i-th item of this CTA. Items are dealt in rounds of gridDim.x, one per
 // CTA, in alternating direction, so that with causal cost falling along the
@@ -81,19 +82,51 @@ __device__ __forceinline__ long long item_index(long long i) {
   const long long G = gridDim.x;
   return i * G + ((i & 1) ? (G - 1 - blockIdx.x) : blockIdx.x);
 }
-__device__ __forceinline__ Item item_of(const AttnParams &p, long long k) {
+// A single problem (attn_fwd, attn_partial): its one block is built from p, so
+// the geometry folds into parameter reads.
+struct SingleProblem {
+  int unused;
+};
+
+__device__ __forceinline__ long long n_items_of(const AttnParams &p, const SingleProblem &) {
+  return static_cast<long long>(p.B) * p.Hq * p.n_qblocks;
+}
+__device__ __forceinline__ long long n_items_of(const AttnParams &, const BlockTable &tbl) {
+  return tbl.item_start[tbl.n];
+}
+__device__ __forceinline__ BlockDesc block_of(const AttnParams &p, const SingleProblem &, int) {
+  return whole_problem(p);
+}
+__device__ __forceinline__ BlockDesc block_of(const AttnParams &, const BlockTable &tbl, int blk) {
+  return tbl.b[blk];
+}
+__device__ __forceinline__ Item item_of(const AttnParams &p, const SingleProblem &, long long k) {
   const long long heads = static_cast<long long>(p.B) * p.Hq;
   const int qi = static_cast<int>(k / heads);
   const int qblock = p.causal ? p.n_qblocks - 1 - qi : qi;
-  return {static_cast<int>(k % heads), qblock * 2 * kRowsPerTile};
+  return {0, static_cast<int>(k % heads), qblock * 2 * kRowsPerTile};
+}
+__device__ __forceinline__ Item item_of(const AttnParams &p, const BlockTable &tbl, long long k) {
+  int lo = 0, hi = tbl.n - 1;  // the last block with item_start <= k
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tbl.item_start[mid] <= k) lo = mid; else hi = mid - 1;
+  }
+  const long long local = k - tbl.item_start[lo];
+  const long long heads = static_cast<long long>(p.B) * p.Hq;
+  const int qi = static_cast<int>(local / heads);
+  const int n_qb = (tbl.b[lo].Sq + 2 * kRowsPerTile - 1) / (2 * kRowsPerTile);
+  const int qblock = p.causal ? n_qb - 1 - qi : qi;
+  return {lo, static_cast<int>(local % heads), qblock * 2 * kRowsPerTile};
 }
 
-template <int D, bool kF32Out>
+template <int D, bool kF32Out, typename Table>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
-                    const __grid_constant__ CUtensorMap tm_o, const AttnParams p) {
+                    const __grid_constant__ CUtensorMap tm_o, const AttnParams p,
+                    const __grid_constant__ Table tbl) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -114,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   int *err = &g_device_error;
-  const long long n_items = static_cast<long long>(p.B) * p.Hq * p.n_qblocks;
+  const long long n_items = n_items_of(p, tbl);
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQFull), 1);
@@ -146,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool skip = *abort_flag != 0;
   // KV tiles query tile t of an item visits (0: none of its rows sees a key)
   auto tiles = [&](const Item &it, int t) -> int {
-    return skip ? 0 : kv_tiles_for(p, it.row0 + t * kRowsPerTile);
+    return skip ? 0 : kv_tiles_for(block_of(p, tbl, it.blk), p.causal, it.row0 + t * kRowsPerTile);
   };
   // TMEM column of S_t / P_t and of O_t for query tile t
   auto tS = [&](int t) -> uint32_t { return tmem + 128u * static_cast<uint32_t>(t); };
@@ -167,16 +200,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       int nq = 0;  // Q tile pairs loaded
       bool ok = true;
       for (long long i = 0, k = item_index(0); k < n_items && ok; k = item_index(++i)) {
-        const Item it = item_of(p, k);
+        const Item it = item_of(p, tbl, k);
         const int n_max = max(tiles(it, 0), tiles(it, 1));
         if (n_max == 0) continue;
         // the previous item's S MMAs must be done reading the Q buffer
         if (nq > 0 && !mbar_wait(bar(kBarQEmpty), (nq - 1) & 1, abort_flag, err)) break;
         mbar_arrive_expect_tx(bar(kBarQFull), 2 * C::kTileBytes);
+        const BlockDesc blk = block_of(p, tbl, it.blk);
+        const int q_row = static_cast<int>(blk.q_row) + it.row0;
+        const int kv_row = static_cast<int>(blk.kv_row);
         for (int t = 0; t < 2; ++t)
           for (int cb = 0; cb < C::kColBlocks; ++cb)
             tma_load_3d(smem_addr(sQ + (t * C::kColBlocks + cb) * kColBlockBytes), &tm_q,
-                        bar(kBarQFull), cb * 64, it.row0 + t * kRowsPerTile, it.bh);
+                        bar(kBarQFull), cb * 64, q_row + t * kRowsPerTile, it.bh);
         ++nq;
         const int b = it.bh / p.Hq, hq = it.bh % p.Hq;
         const int kv_head = b * p.Hkv + hq / (p.Hq / p.Hkv);
@@ -192,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const CUtensorMap *map = which ? &tm_v : &tm_k;
             for (int cb = 0; cb < C::kColBlocks; ++cb)
               tma_load_3d(smem_addr(sRing + (slot * C::kColBlocks + cb) * kColBlockBytes), map,
-                          bar(kBarFull + slot), cb * 64, j * kRowsPerTile, kv_head);
+                          bar(kBarFull + slot), cb * 64, kv_row + j * kRowsPerTile, kv_head);
           }
         }
       }
@@ -215,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g[2] = {0, 0};     // KV steps done by each query tile over earlier items
       bool ok = true;
       for (long long i = 0, k = item_index(0); k < n_items && ok; k = item_index(++i)) {
-        const Item it = item_of(p, k);
+        const Item it = item_of(p, tbl, k);
         const int n_t[2] = {tiles(it, 0), tiles(it, 1)};
         const int n_max = max(n_t[0], n_t[1]);
         if (n_max == 0) continue;
@@ -292,19 +328,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     int g = 0;       // KV steps of this tile over earlier items
     uint32_t u = 0;  // earlier items in which this tile visited a KV tile
     for (long long i = 0, k = item_index(0); k < n_items; k = item_index(++i)) {
-      const Item it = item_of(p, k);
+      const Item it = item_of(p, tbl, k);
+      const BlockDesc blk = block_of(p, tbl, it.blk);
+      const int out_head = blk.part * p.B * p.Hq + it.bh;  // head of O / lse written
       const int tile_first = it.row0 + t * kRowsPerTile;
       const int n = tiles(it, t);
       if (n == 0) {
-        write_empty_rows<D, kF32Out>(p, it.bh, tile_first, kRowsPerTile, threadIdx.x & 127, 128);
+        write_empty_rows<D, kF32Out>(p, blk, out_head, tile_first, kRowsPerTile,
+                                     threadIdx.x & 127, 128);
         continue;
       }
       const int row = tile_first + row_in_tile;
-      const EpilogueStore store{&tm_o, stage, 1 + t, it.bh};
+      const EpilogueStore store{&tm_o, stage, 1 + t, out_head};
       const bool ok = softmax_row<D, kF32Out>(
-          p, row, tile_first, n, tS(t) + lane_off, tO(t) + lane_off, bar(kBarSFull + t),
-          bar(kBarOFull + t), g, u & 1u, static_cast<size_t>(it.bh) * p.Sq + row, abort_flag,
-          err, store, [&] {
+          p, blk, row, tile_first, n, tS(t) + lane_off, tO(t) + lane_off, bar(kBarSFull + t),
+          bar(kBarOFull + t), g, u & 1u,
+          static_cast<size_t>(out_head) * p.o_rows + static_cast<size_t>(blk.o_row + row),
+          abort_flag, err, store, [&] {
             __syncwarp();
             if (lane == 0) mbar_arrive(pfull);  // one arrival per warp
           });
@@ -338,18 +378,30 @@ int sm_count() {
   return n;
 }
 
-template <int D, bool kF32Out>
+template <int D, bool kF32Out, typename Table>
 cudaError_t launch_typed(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                         const CUtensorMap &to, const AttnParams &p, cudaStream_t stream) {
-  auto kernel = attn_fwd_kernel<D, kF32Out>;
+                         const CUtensorMap &to, const AttnParams &p, const Table &tbl,
+                         long long n_items, cudaStream_t stream) {
+  auto kernel = attn_fwd_kernel<D, kF32Out, Table>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg<D>::kSmemBytes);
   if (e != cudaSuccess) return e;
+  if (n_items == 0) return cudaSuccess;
   // persistent: one CTA per SM (or per work item, if there are fewer)
-  const long long n_items = static_cast<long long>(p.B) * p.Hq * p.n_qblocks;
   const long long grid = n_items < sm_count() ? n_items : sm_count();
-  kernel<<<static_cast<unsigned>(grid), kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, to, p);
+  kernel<<<static_cast<unsigned>(grid), kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, to, p,
+                                                                               tbl);
   return cudaGetLastError();
+}
+
+template <typename Table>
+cudaError_t launch_dispatch(int D, bool f32_out, const CUtensorMap &tq, const CUtensorMap &tk,
+                            const CUtensorMap &tv, const CUtensorMap &to, const AttnParams &p,
+                            const Table &tbl, long long n_items, cudaStream_t stream) {
+  if (D == 128) return f32_out ? launch_typed<128, true>(tq, tk, tv, to, p, tbl, n_items, stream)
+                               : launch_typed<128, false>(tq, tk, tv, to, p, tbl, n_items, stream);
+  return f32_out ? launch_typed<64, true>(tq, tk, tv, to, p, tbl, n_items, stream)
+                 : launch_typed<64, false>(tq, tk, tv, to, p, tbl, n_items, stream);
 }
 
 }  // namespace
@@ -375,10 +427,15 @@ cudaError_t launch_attention(int D, bool f32_out, bool pair, const CUtensorMap &
                              const AttnParams &p, cudaStream_t stream) {
   if (pair) return f32_out ? pair2sm::launch_pair<true>(tq, tk, tv, p, stream)
                            : pair2sm::launch_pair<false>(tq, tk, tv, p, stream);
-  if (D == 128) return f32_out ? launch_typed<128, true>(tq, tk, tv, to, p, stream)
-                               : launch_typed<128, false>(tq, tk, tv, to, p, stream);
-  return f32_out ? launch_typed<64, true>(tq, tk, tv, to, p, stream)
-                 : launch_typed<64, false>(tq, tk, tv, to, p, stream);
+  return launch_dispatch(D, f32_out, tq, tk, tv, to, p, SingleProblem{0},
+                         static_cast<long long>(p.B) * p.Hq * p.n_qblocks, stream);
+}
+
+cudaError_t launch_attention_blocks(int D, bool f32_out, const CUtensorMap &tq,
+                                    const CUtensorMap &tk, const CUtensorMap &tv,
+                                    const CUtensorMap &to, const AttnParams &p,
+                                    const BlockTable &tbl, cudaStream_t stream) {
+  return launch_dispatch(D, f32_out, tq, tk, tv, to, p, tbl, tbl.item_start[tbl.n], stream);
 }
 
 // A one-CTA kernel waiting on an mbarrier that nothing ever arrives at, with

@@ -17,6 +17,29 @@ struct AttnParams {
   int causal;
   int n_qblocks;      // ceil(Sq / 256): two 128-row query tiles per CTA
   int skip_empty;     // rows that see no key: write lse = -inf only, leave O untouched
+  long long o_rows;   // rows per head of O and lse (Sq for a single problem)
+};
+
+// One block of attention: the queries in rows [q_row, q_row + Sq) of Q (per
+// head) against the keys and values in rows [kv_row, kv_row + Skv) of K / V,
+// written to rows [o_row, o_row + Sq) of part `part` of O and lse (O viewed as
+// [parts][B * Hq heads][rows][D]). q_pos / kv_pos are the global positions of
+// query row 0 and key 0 (the causal mask compares them).
+struct BlockDesc {
+  long long q_row, kv_row, o_row;
+  long long q_pos, kv_pos;
+  int Sq, Skv;
+  int part;
+};
+
+// The blocks of one launch, passed by value in the kernel parameters.
+// item_start[i] is the first work item of block i (items: B * Hq heads times
+// ceil(Sq / 256) query blocks per block), item_start[n] the total.
+constexpr int kMaxLaunchBlocks = 64;
+struct BlockTable {
+  int n;
+  long long item_start[kMaxLaunchBlocks + 1];
+  BlockDesc b[kMaxLaunchBlocks];
 };
 
 // Whether attention with head dim D runs on SM pairs (2-SM MMAs). The pair
@@ -30,6 +53,13 @@ bool attention_uses_pair(int D);
 cudaError_t launch_attention(int D, bool f32_out, bool pair, const CUtensorMap &tm_q,
                              const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                              const CUtensorMap &tm_o, const AttnParams &p, cudaStream_t stream);
+
+// The single-SM persistent kernel over a table of blocks (row ranges of the
+// maps' row dimension; p's Sq / Skv / q_off / kv_off / n_qblocks are unused).
+cudaError_t launch_attention_blocks(int D, bool f32_out, const CUtensorMap &tm_q,
+                                    const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                                    const CUtensorMap &tm_o, const AttnParams &p,
+                                    const BlockTable &tbl, cudaStream_t stream);
 
 cudaError_t launch_lse_merge(const float *o_parts, const float *lse_parts, int P, long long nrows,
                              int D, void *o, bool bf16_out, float *lse, cudaStream_t stream);

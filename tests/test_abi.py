@@ -32,7 +32,7 @@ def test_header_declares_the_boundary():
     assert declared_functions() == sorted(["attn_fwd", "attn_partial", "lse_merge", "attn_query_device_error",
                                            "attn_status_string", "attn_last_cuda_error",
                                            "attn_ring_fwd_static", "attn_debug_expire_wait",
-                                           "attn_debug_exp2"])
+                                           "attn_debug_exp2", "attn_partial_blocks", "attn_fwd_varlen"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -112,3 +112,48 @@ def test_lse_merge_argument_checks(lib):
     assert merge(parts=0) == 1
     assert merge(parts=FAKE + 4) == 1
     assert merge(S=0) == 0
+
+
+def test_attn_block_layout_matches_the_header():
+    from sequence_attn_fwd_gb300._lib import AttnBlock
+
+    assert ctypes.sizeof(AttnBlock) == 56  # five int64 and three int32, 8-byte aligned
+    text = open(HEADER).read()
+    assert "long long q_row, kv_row, o_row;" in text and "int part;" in text
+
+
+def test_attn_partial_blocks_argument_checks(lib):
+    from sequence_attn_fwd_gb300._lib import AttnBlock
+
+    def run(blocks, q_rows=512, kv_rows=512, o_rows=512, n_parts=2, D=128, flags=0):
+        arr = (AttnBlock * max(len(blocks), 1))(*[AttnBlock(*b) for b in blocks])
+        return lib.attn_partial_blocks(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.addressof(arr), len(blocks), 1, 2, 1,
+                                       q_rows, kv_rows, o_rows, n_parts, D, 1, ctypes.c_float(0.1), flags, None)
+
+    ok = (0, 0, 0, 0, 0, 256, 256, 0)
+    assert run([]) == 0
+    assert run([ok, (0, 0, 200, 0, 0, 100, 100, 0)]) == 1  # output rows 200.. overlap 0..256 in part 0
+    assert run([(0, 0, 0, 0, 0, 256, 256, 2)]) == 1  # part out of range
+    assert run([(300, 0, 0, 0, 0, 256, 256, 0)]) == 1  # queries past q_rows
+    assert run([(0, 300, 0, 0, 0, 256, 256, 0)]) == 1  # keys past kv_rows
+    assert run([(0, 0, 300, 0, 0, 256, 256, 0)]) == 1  # outputs past o_rows
+    assert run([(0, 0, 0, 0, 0, -1, 256, 0)]) == 1
+    assert run([ok], D=96) == 2
+    assert run([ok], flags=4) == 1
+    assert lib.attn_partial_blocks(FAKE, FAKE, FAKE, FAKE, FAKE, None, 3, 1, 2, 1, 8, 8, 8, 1, 128, 1,
+                                   ctypes.c_float(0.1), 0, None) == 1  # null block array
+
+
+def test_attn_fwd_varlen_argument_checks(lib):
+    def run(cq, ck, Hq=2, Hkv=1, D=128):
+        aq = (ctypes.c_longlong * len(cq))(*cq)
+        ak = (ctypes.c_longlong * len(ck))(*ck)
+        return lib.attn_fwd_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.addressof(aq), ctypes.addressof(ak),
+                                   len(cq) - 1, Hq, Hkv, D, 1, ctypes.c_float(0.1), None)
+
+    assert run([0], [0]) == 0  # no sequence
+    assert run([0, 0, 0], [0, 5, 9]) == 0  # no query row
+    assert run([1, 5], [0, 5]) == 1  # must start at 0
+    assert run([0, 5, 3], [0, 5, 9]) == 1  # decreasing
+    assert run([0, 5], [0, 5], Hq=3, Hkv=2) == 1
+    assert run([0, 5], [0, 5], D=32) == 2

@@ -199,22 +199,107 @@ def test_lse_merge_part_counts(sa, P, D):
     check_lse(l, lse_ref, tol=1e-5)
 
 
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "per_block"])
 @pytest.mark.parametrize("layout", ["contiguous", "zigzag"])
 @pytest.mark.parametrize("shape", [(1, 4, 2, 2048, 128, 4), (2, 3, 1, 1536, 64, 3), (1, 2, 2, 1200, 128, 3)],
                          ids=["gqa_s2048_p4", "d64_s1536_p3", "ragged_chunks_s1200_p3"])
-def test_emulated_ring_layouts_against_oracle(sa, layout, shape):
+def test_emulated_ring_layouts_against_oracle(sa, layout, shape, fused):
     """P emulated ring devices, each computing the blocks the schedule gives it
-    hop by hop (attn_partial at global offsets) and merging per query chunk:
-    the assembled output is the single-pass causal attention."""
+    hop by hop (one grouped launch per device and hop, or one attn_partial per
+    block) and merging per query chunk: the assembled output is the
+    single-pass causal attention."""
     B, Hq, Hkv, S, D, P = shape
     q, k, v = workloads.make_qkv(adhoc(B, Hq, Hkv, S, D, True, seed=55))
     o_ref, lse_ref = oracle.attention(q, k, v, True)
-    ring = sa.EmulatedRing(*to_dev(q, k, v), P=P, layout=layout, causal=True)
+    ring = sa.EmulatedRing(*to_dev(q, k, v), P=P, layout=layout, causal=True, fused=fused)
     hop_ms, merge_ms = ring.run(timing=True)
     assert len(hop_ms) == P and all(len(r) == P for r in hop_ms) and len(merge_ms) == P
     o, lse = ring.output()
     check_o(o, o_ref)
     check_lse(lse, lse_ref)
+
+
+def packed(Hq, Hkv, total_q, total_k, D, seed):
+    """Packed [H, total, D] bf16 tensors from the seeded generator."""
+    q, _, _ = workloads.make_qkv(adhoc(1, Hq, Hq, max(total_q, 1), D, False, seed=seed))
+    _, k, v = workloads.make_qkv(adhoc(1, Hkv, Hkv, max(total_k, 1), D, False, seed=seed + 1))
+    return q[0, :, :total_q].contiguous(), k[0, :, :total_k].contiguous(), v[0, :, :total_k].contiguous()
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("D,Hq,Hkv", [(128, 4, 2), (64, 3, 3)])
+def test_attn_fwd_varlen_against_oracle(sa, causal, D, Hq, Hkv):
+    """Packed sequences of lengths 1 .. 517 (one empty), each compared with the
+    oracle on its own rows; a sequence's last tile ends inside the next one's."""
+    lens = [1, 127, 128, 0, 129, 300, 517, 64]
+    cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
+    q, k, v = packed(Hq, Hkv, cu[-1], cu[-1], D, seed=91)
+    o, lse = sa.attn_fwd_varlen(*to_dev(q, k, v), cu, cu, causal=causal)
+    torch.cuda.synchronize()
+    for s_, (a, b) in enumerate(zip(cu[:-1], cu[1:])):
+        if b == a:
+            continue
+        o_ref, lse_ref = oracle.attention(q[None, :, a:b].contiguous(), k[None, :, a:b].contiguous(),
+                                          v[None, :, a:b].contiguous(), causal)
+        check_o(o[None, :, a:b], o_ref)
+        check_lse(lse[None, :, a:b], lse_ref)
+
+
+def test_attn_fwd_varlen_bottom_right_causal(sa):
+    """Fewer query rows than keys: the mask is aligned at the bottom right
+    (query i sees keys j <= i + Skv - Sq); more query rows than keys: the first
+    rows see nothing (O = 0, lse = -inf)."""
+    cq, ck = [0, 100, 150, 350], [0, 300, 350, 450]
+    Hq, Hkv, D = 2, 1, 128
+    q, k, v = packed(Hq, Hkv, cq[-1], ck[-1], D, seed=93)
+    o, lse = sa.attn_fwd_varlen(*to_dev(q, k, v), cq, ck, causal=True)
+    torch.cuda.synchronize()
+    for (qa, qb), (ka, kb) in zip(zip(cq[:-1], cq[1:]), zip(ck[:-1], ck[1:])):
+        sq, sk = qb - qa, kb - ka
+        o_ref, lse_ref = oracle.attention(q[None, :, qa:qb].contiguous(), k[None, :, ka:kb].contiguous(),
+                                          v[None, :, ka:kb].contiguous(), True, q_off=sk - sq, kv_off=0)
+        check_o(o[None, :, qa:qb], o_ref)
+        check_lse(lse[None, :, qa:qb], lse_ref)
+    assert torch.isneginf(lse[:, 150:250]).all()  # the 3rd sequence: rows i < Sq - Skv = 100 see no key
+
+
+def test_attn_partial_blocks_against_oracle(sa):
+    """Ragged blocks at arbitrary rows and positions, overlapping query ranges,
+    two output parts; every block's rows compared with the oracle."""
+    B, Hq, Hkv, D = 2, 4, 2, 128
+    q_rows, kv_rows, o_rows = 700, 900, 640
+    q, k, v = workloads.make_qkv(adhoc(B, Hq, Hkv, max(q_rows, kv_rows), D, False, seed=97))
+    q, k, v = q[:, :, :q_rows].contiguous(), k[:, :, :kv_rows].contiguous(), v[:, :, :kv_rows].contiguous()
+    blocks = [(0, 0, 0, 0, 0, 300, 400, 0),
+              (300, 400, 300, 300, 400, 340, 500, 0),
+              (0, 100, 0, 50, 100, 257, 333, 1),
+              (450, 0, 300, 1000, 0, 129, 900, 1),
+              (600, 777, 500, 5, 900, 100, 123, 1)]
+    for causal in (True, False):
+        out = torch.full((2, B, Hq, o_rows, D), 7.0, dtype=torch.float32, device="cuda")
+        lse = torch.full((2, B, Hq, o_rows), 7.0, dtype=torch.float32, device="cuda")
+        sa.attn_partial_blocks(*to_dev(q, k, v), blocks, n_parts=2, o_rows=o_rows, causal=causal, out=out, lse=lse)
+        torch.cuda.synchronize()
+        written = torch.zeros((2, o_rows), dtype=torch.bool)
+        for qr, kr, orow, qp, kp, sq, sk, part in blocks:
+            o_ref, lse_ref = oracle.attention(q[:, :, qr:qr + sq].contiguous(), k[:, :, kr:kr + sk].contiguous(),
+                                              v[:, :, kr:kr + sk].contiguous(), causal, q_off=qp, kv_off=kp)
+            check_o(out[part, :, :, orow:orow + sq], o_ref, bf16_out=False)
+            check_lse(lse[part, :, :, orow:orow + sq], lse_ref)
+            written[part, orow:orow + sq] = True
+        # rows no block writes keep their contents
+        for part in range(2):
+            free = (~written[part]).nonzero().flatten().tolist()
+            if free:
+                assert (out[part, :, :, free] == 7.0).all() and (lse[part, :, :, free] == 7.0).all()
+
+
+def test_ring_grouped_launch_is_bitwise_the_per_chunk_launches(sa):
+    q, k, v = to_dev(*workloads.make_qkv(adhoc(1, 4, 4, 2048, 128, True, seed=99)))
+    o1, l1 = sa.ring_attn_fwd(q, k, v, P=4, causal=True)
+    o2, l2 = sa.ring_attn_fwd(q, k, v, P=4, causal=True, grouped=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
 # ----------------------------------------------------------------- full-size workloads
@@ -223,7 +308,7 @@ def run_workload(sa, w, q, k, v):
     """The launch configuration the benchmark times for this workload."""
     if w.P == 1:
         return sa.attn_fwd(q, k, v, causal=w.causal)
-    return sa.ring_attn_fwd(q, k, v, P=w.P, causal=w.causal)
+    return sa.ring_attn_fwd(q, k, v, P=w.P, causal=w.causal, grouped=True)
 
 
 @pytest.mark.parametrize("name", list(W))

@@ -95,6 +95,7 @@ def merge_algorithmic_bytes(w: workloads.Workload, out_bytes: int = 2) -> int:
 KERNEL_SOURCES = {
     "attn_partial": ["attn_kernel.cu", "attn_common.cuh", "ptx.cuh"],
     "attn_partial_blocks": ["attn_kernel.cu", "attn_common.cuh", "ptx.cuh"],
+    "attn_fwd_varlen": ["attn_kernel.cu", "attn_common.cuh", "ptx.cuh"],
     "attn_fwd": ["attn_kernel.cu", "attn_common.cuh", "ptx.cuh"],
     "lse_merge": ["lse_merge.cu"],
 }
@@ -221,10 +222,18 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int):
         o_parts = torch.empty((P, B, Hq, S, D), dtype=torch.float32, device=dev)
         lse_parts = torch.empty((P, B, Hq, S), dtype=torch.float32, device=dev)
     grouped = P > 1 and args.partials == "grouped"
+    cu = workloads.cu_seqlens(w) if w.varlen else None
     launches_per_step = (2 if grouped else P + 1) if P > 1 else 1
     chunk_blocks = [(0, j * C, 0, 0, j * C, S, C, j) for j in range(P)]
 
     def step(qq, kk, vv, ev=None):
+        if w.varlen:  # packed sequences: [Hq, total, D] views of the B = 1 tensors
+            if ev:
+                ev[0].record(stream)
+            sa.attn_fwd_varlen(qq[0], kk[0], vv[0], cu, cu, causal=w.causal, out=o[0], lse=lse[0])
+            if ev:
+                ev[1].record(stream)
+            return
         if P == 1:
             if ev:
                 ev[0].record(stream)
@@ -318,9 +327,11 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int):
     attn_avg_ms = statistics.mean(attn_ms) / n_attn  # per launch
     flops_per_launch = F / n_attn
     achieved = flops_per_launch / (attn_avg_ms * 1e-3) / 1e12
-    entry = "attn_partial_blocks" if grouped else ("attn_partial" if P > 1 else "attn_fwd")
+    entry = "attn_partial_blocks" if grouped else ("attn_partial" if P > 1 else
+                                                   ("attn_fwd_varlen" if w.varlen else "attn_fwd"))
     what = {"attn_partial_blocks": f"<f32 out> (attn_partial_blocks: the {P} key chunks in one launch)",
-            "attn_partial": "<f32 out> (attn_partial)", "attn_fwd": "<bf16 out>"}[entry]
+            "attn_partial": "<f32 out> (attn_partial)", "attn_fwd": "<bf16 out>",
+            "attn_fwd_varlen": f"<bf16 out> (attn_fwd_varlen: {len(cu) - 1 if cu else 0} packed sequences)"}[entry]
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"],
                 "traffic": measured_traffic(entry, w.name),
@@ -355,12 +366,30 @@ def oracle_sample(w: workloads.Workload, budget_s: float, q=None, k=None, v=None
     if q is None:
         q, k, v = workloads.make_qkv(w)
     threads = oracle.default_threads()
-    rows = workloads.sample_query_rows(w, n=min(w.S, 256))
     g = w.Hq // w.Hkv
     flops = 0.0
     done = 0
     calls = 0
     t0 = time.perf_counter()
+    if w.varlen:  # one head of one sequence per call, up to 256 seeded rows of it, sequences in turn
+        cu = workloads.cu_seqlens(w)
+        rng = np.random.Generator(np.random.PCG64(w.seed))
+        while True:
+            s, h = divmod(calls, w.Hq)
+            s %= len(cu) - 1
+            a, b = cu[s], cu[s + 1]
+            r = np.sort(rng.choice(b - a, size=min(256, b - a), replace=False)).astype(np.int64)[None]
+            oracle.attention(q[:, h:h + 1, a:b], k[:, h // g:h // g + 1, a:b], v[:, h // g:h // g + 1, a:b],
+                             w.causal, rows=r, threads=threads)
+            nvis = r[0] + 1 if w.causal else np.full(r.shape[1], b - a)
+            flops += 4.0 * w.D * float(nvis.sum())
+            done += r.shape[1]
+            calls += 1
+            if time.perf_counter() - t0 >= budget_s or (max_calls and calls >= max_calls):
+                break
+        secs = time.perf_counter() - t0
+        return flops / secs / 1e12, secs, done, threads
+    rows = workloads.sample_query_rows(w, n=min(w.S, 256))
     while True:
         bh = calls % (w.B * w.Hq)
         b, h = divmod(bh, w.Hq)
@@ -390,7 +419,8 @@ def run_reference(args, w):
         heads += n
     elapsed = time.perf_counter() - t0
     value = sum(rates) / len(rates)
-    sample = (f"{heads} seeded query rows (256 per (batch, head), heads in turn) over {args.steps} steps "
+    unit = "(sequence, head), sequences and heads" if w.varlen else "(batch, head), heads"
+    sample = (f"{heads} seeded query rows (up to 256 per {unit} in turn) over {args.steps} steps "
               f"(about {args.reference_budget:.0f} s of CPU work per step); fp64 definition")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed * 1e3 / args.steps,
@@ -495,8 +525,9 @@ def main(argv=None):
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
             val, secs, heads, threads = oracle_sample(w, args.cpu_baseline_budget)
+            unit = "(sequence, head), sequences and heads" if w.varlen else "(batch, head), heads"
             cpu = {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                   "sample": f"{heads} seeded query rows of the workload (256 per (batch, head), heads "
+                   "sample": f"{heads} seeded query rows of the workload (up to 256 per {unit} "
                              f"in turn; {secs:.1f} s), fp64 definition"}
         line = {"metric": METRIC, "value": r["value"], "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True,

@@ -90,7 +90,14 @@ def test_workload_sizes_match_the_stated_configurations():
     W = workloads.WORKLOADS
     assert [(w.B, w.Hq, w.Hkv, w.S, w.D, w.causal, w.P) for w in W.values()] == [
         (1, 2, 2, 256, 64, False, 1), (2, 32, 32, 4096, 128, True, 8), (1, 28, 4, 32768, 128, True, 1),
-        (2, 32, 32, 8192, 128, True, 16), (1, 32, 8, 131072, 128, True, 16)]
+        (2, 32, 32, 8192, 128, True, 16), (1, 32, 8, 131072, 128, True, 16), (1, 32, 8, 65536, 128, True, 1)]
+    v = W["varlen_hq32hkv8t65536d128_causal"]
+    lens = workloads.seq_lens(v)
+    assert lens.sum() == v.S and lens.min() >= 1 and lens[:-1].min() >= 128 and lens.max() <= 8192
+    assert len(lens) > 20 and np.array_equal(lens, workloads.seq_lens(v))  # seeded
+    cu = workloads.cu_seqlens(v)
+    assert cu[0] == 0 and cu[-1] == v.S and len(cu) == len(lens) + 1
+    assert math.isclose(v.attention_flops(), 2.0 * 32 * 128 * float((lens.astype(float) ** 2).sum()))
     w = W["gqa_b1hq28hkv4s32768d128_causal"]
     pos = workloads.boost_positions(w)
     assert len(pos) == 327 and len(np.unique(pos)) == 327

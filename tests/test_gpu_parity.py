@@ -306,6 +306,10 @@ def test_ring_grouped_launch_is_bitwise_the_per_chunk_launches(sa):
 
 def run_workload(sa, w, q, k, v):
     """The launch configuration the benchmark times for this workload."""
+    if w.varlen:
+        cu = workloads.cu_seqlens(w)
+        o, lse = sa.attn_fwd_varlen(q[0], k[0], v[0], cu, cu, causal=w.causal)
+        return o[None], lse[None]
     if w.P == 1:
         return sa.attn_fwd(q, k, v, causal=w.causal)
     return sa.ring_attn_fwd(q, k, v, P=w.P, causal=w.causal, grouped=True)
@@ -315,6 +319,8 @@ def run_workload(sa, w, q, k, v):
 def test_full_size_workload_sampled_rows(sa, name):
     w = W[name]
     q, k, v = workloads.make_qkv(w)
+    if w.varlen:
+        return check_varlen_workload(sa, w, q, k, v)
     rows = workloads.sample_query_rows(w, n=w.sample_rows or 32)
     # chunk boundaries and the last row are checked too
     extra = np.array(sorted({0, w.chunk - 1, w.chunk, w.S - 1} & set(range(w.S))), dtype=np.int64)
@@ -325,6 +331,32 @@ def test_full_size_workload_sampled_rows(sa, name):
     o, lse = run_workload(sa, w, qd, kd, vd)
     check_o(gather_rows(o, rows), o_ref)
     check_lse(gather_rows(lse, rows), lse_ref)
+    del o, lse, qd, kd, vd
+    torch.cuda.empty_cache()
+
+
+def check_varlen_workload(sa, w, q, k, v):
+    """Sampled rows of a packed workload (the same for every head: 32 seeded
+    rows plus each sequence's first and last row), each checked against the
+    oracle on its own sequence."""
+    cu = workloads.cu_seqlens(w)
+    rng = np.random.default_rng(w.seed)
+    rows = set(rng.choice(w.S, size=32, replace=False).tolist())
+    rows |= {a for a in cu[:-1]} | {b - 1 for b in cu[1:]}
+    rows = np.array(sorted(rows), dtype=np.int64)
+    qd, kd, vd = to_dev(q, k, v)
+    o, lse = run_workload(sa, w, qd, kd, vd)
+    torch.cuda.synchronize()
+    seq = np.searchsorted(np.array(cu), rows, side="right") - 1
+    for s in np.unique(seq):
+        a, b = cu[s], cu[s + 1]
+        local = rows[seq == s] - a
+        o_ref, lse_ref = oracle.attention(q[:, :, a:b].contiguous(), k[:, :, a:b].contiguous(),
+                                          v[:, :, a:b].contiguous(), w.causal,
+                                          rows=np.tile(local, (w.Hq, 1)))
+        idx = torch.as_tensor(a + local, device=o.device)
+        check_o(o[:, :, idx], o_ref)
+        check_lse(lse[:, :, idx], lse_ref)
     del o, lse, qd, kd, vd
     torch.cuda.empty_cache()
 

@@ -18,7 +18,13 @@ Recipe (every draw is reproducible from the integer seed):
   * "extra" spawns the stream for the key-boost positions (a distinct
     sample of floor(frac * S) sequence positions whose keys are multiplied
     by 2, exact in bf16, for every batch and KV head), the stream for the
-    sampled query rows, and the stream for synthetic merge partials.
+    sampled query rows, the stream for synthetic merge partials, and the
+    stream for the sequence lengths of a packed (varlen) workload.
+  * A packed workload (B = 1, S = total tokens) draws sequence lengths
+    round(exp(N(ln 1536, 0.8^2))) clipped to [128, 8192] until the total is
+    reached, the last one cut to fit: a training-style length mix with many
+    short and some long sequences. Q, K and V are drawn as for one sequence
+    of S tokens; the sequences are consecutive row ranges of it.
 """
 from __future__ import annotations
 
@@ -45,6 +51,7 @@ class Workload:
     seed: int
     k_boost_frac: float = 0.0  # fraction of positions whose keys are doubled
     sample_rows: int = 0  # query rows per (batch, head) checked against the oracle; 0 = all
+    varlen: bool = False  # packed sequences of seeded lengths (B = 1, S = total tokens)
 
     @property
     def chunk(self) -> int:
@@ -55,8 +62,13 @@ class Workload:
         return 1.0 / math.sqrt(self.D)
 
     def attention_flops(self) -> float:
-        """Causal-adjusted FLOPs 4*B*Hq*S^2*D (halved when causal)."""
-        f = 4.0 * self.B * self.Hq * self.S * self.S * self.D
+        """Causal-adjusted FLOPs 4*B*Hq*S^2*D (halved when causal); a packed
+        workload sums this over its sequences."""
+        if self.varlen:
+            lens = seq_lens(self).astype(np.float64)
+            f = 4.0 * self.Hq * self.D * float((lens * lens).sum())
+        else:
+            f = 4.0 * self.B * self.Hq * self.S * self.S * self.D
         return f * 0.5 if self.causal else f
 
 
@@ -71,6 +83,8 @@ WORKLOADS = {
         Workload("merge16_b2h32s8192d128_causal", 2, 32, 32, 8192, 128, True, 16, 1004),
         Workload("ring16_b1hq32hkv8s131072d128_causal", 1, 32, 8, 131072, 128, True, 16, 1005,
                  sample_rows=64),
+        Workload("varlen_hq32hkv8t65536d128_causal", 1, 32, 8, 65536, 128, True, 1, 1006,
+                 varlen=True),
     ]
 }
 
@@ -125,6 +139,25 @@ def sample_query_rows(w: Workload, n: int | None = None, S: int | None = None) -
     rng = np.random.Generator(np.random.PCG64(_streams(w.seed)[3].spawn(3)[1]))
     rows = np.stack([np.sort(rng.choice(S, size=n, replace=False)) for _ in range(w.B * w.Hq)])
     return rows.astype(np.int64)
+
+
+def seq_lens(w: Workload) -> np.ndarray:
+    """Sequence lengths of a packed workload (int64, summing to w.S); [S] otherwise."""
+    if not w.varlen:
+        return np.array([w.S], dtype=np.int64)
+    rng = np.random.Generator(np.random.PCG64(_streams(w.seed)[3].spawn(4)[3]))
+    lens, total = [], 0
+    while total < w.S:
+        n = int(min(max(round(math.exp(rng.normal(math.log(1536.0), 0.8))), 128), 8192))
+        n = min(n, w.S - total)
+        lens.append(n)
+        total += n
+    return np.array(lens, dtype=np.int64)
+
+
+def cu_seqlens(w: Workload) -> list[int]:
+    """[0, L0, L0 + L1, ..., S] for a packed workload."""
+    return [0] + np.cumsum(seq_lens(w)).tolist()
 
 
 def make_partials(P: int, B: int, H: int, S: int, D: int, seed: int, causal: bool = True):

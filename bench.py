@@ -26,6 +26,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -96,6 +97,7 @@ KERNEL_SOURCES = {
     "attn_partial": ["attn_kernel.cu", "attn_common.cuh", "ptx.cuh"],
     "attn_partial_blocks": ["attn_kernel.cu", "attn_common.cuh", "ptx.cuh"],
     "attn_fwd_varlen": ["attn_kernel.cu", "attn_common.cuh", "ptx.cuh"],
+    "attn_fwd_fp8": ["attn_kernel.cu", "attn_common.cuh", "ptx.cuh"],
     "attn_fwd": ["attn_kernel.cu", "attn_common.cuh", "ptx.cuh"],
     "lse_merge": ["lse_merge.cu"],
 }
@@ -221,12 +223,28 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int):
     if P > 1:
         o_parts = torch.empty((P, B, Hq, S, D), dtype=torch.float32, device=dev)
         lse_parts = torch.empty((P, B, Hq, S), dtype=torch.float32, device=dev)
+    fp8 = args.dtype == "e4m3"
+    if fp8:  # inputs on the e4m3 grid with power-of-two per-tensor scales (untimed preparation)
+        if w.varlen or P > 1 or D != 128:
+            raise SystemExit("--dtype e4m3 runs single-pass head-dim-128 workloads")
+        sc = [2.0 ** math.ceil(math.log2(float(t.abs().max()) / 448.0)) for t in (q_h, k_h, v_h)]
+        # the step's inputs become the e4m3 tensors (V transposed), on the device and the host
+        q, k, v = (sa.quantize_e4m3(q, sc[0]), sa.quantize_e4m3(k, sc[1]),
+                   sa.quantize_e4m3(v, sc[2]).transpose(2, 3).contiguous())
+        q_h, k_h, v_h = q.cpu(), k.cpu(), v.cpu()
     grouped = P > 1 and args.partials == "grouped"
     cu = workloads.cu_seqlens(w) if w.varlen else None
     launches_per_step = (2 if grouped else P + 1) if P > 1 else 1
     chunk_blocks = [(0, j * C, 0, 0, j * C, S, C, j) for j in range(P)]
 
     def step(qq, kk, vv, ev=None):
+        if fp8:  # qq, kk, vv: e4m3 Q, K and V^T
+            if ev:
+                ev[0].record(stream)
+            sa.attn_fwd_fp8(qq, kk, vv, sc[0], sc[1], sc[2], causal=w.causal, out=o, lse=lse)
+            if ev:
+                ev[1].record(stream)
+            return
         if w.varlen:  # packed sequences: [Hq, total, D] views of the B = 1 tensors
             if ev:
                 ev[0].record(stream)
@@ -328,16 +346,21 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int):
     flops_per_launch = F / n_attn
     achieved = flops_per_launch / (attn_avg_ms * 1e-3) / 1e12
     entry = "attn_partial_blocks" if grouped else ("attn_partial" if P > 1 else
-                                                   ("attn_fwd_varlen" if w.varlen else "attn_fwd"))
+                                                   ("attn_fwd_varlen" if w.varlen else
+                                                    ("attn_fwd_fp8" if fp8 else "attn_fwd")))
     what = {"attn_partial_blocks": f"<f32 out> (attn_partial_blocks: the {P} key chunks in one launch)",
             "attn_partial": "<f32 out> (attn_partial)", "attn_fwd": "<bf16 out>",
-            "attn_fwd_varlen": f"<bf16 out> (attn_fwd_varlen: {len(cu) - 1 if cu else 0} packed sequences)"}[entry]
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"],
+            "attn_fwd_varlen": f"<bf16 out> (attn_fwd_varlen: {len(cu) - 1 if cu else 0} packed sequences)",
+            "attn_fwd_fp8": "<bf16 out, e4m3 Q/K/V/P> (attn_fwd_fp8)"}[entry]
+    # e4m3 MMAs: the measured bf16 peak times the nominal e4m3 / bf16 ratio (4.5 / 2.25)
+    peak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak,
                 "traffic": measured_traffic(entry, w.name),
                 "kernel": ("attn_fwd_2sm_kernel" if D == 128 and os.environ.get("SEQATTN_ATTN_KERNEL") == "2sm"
                            and not grouped else f"attn_fwd_kernel<{D}>") + what,
-                "peak_source": f"{peak_src} bf16 burst", "launch_ms": attn_avg_ms}
+                "peak_source": f"{peak_src} bf16 burst" + (" x 2 (nominal e4m3 / bf16 ratio)" if fp8 else ""),
+                "launch_ms": attn_avg_ms}
     merge = None
     if merge_ms:
         mb = merge_algorithmic_bytes(w)
@@ -485,6 +508,8 @@ def main(argv=None):
     ap.add_argument("--cpu-baseline-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "e4m3"],
+                    help="e4m3: Q, K, V quantised to FP8 with per-tensor scales (attn_fwd_fp8)")
     ap.add_argument("--partials", default="grouped", choices=["grouped", "per-chunk"],
                     help="ring workloads: the P chunks' partials in one attn_partial_blocks launch "
                          "(default) or one attn_partial launch per chunk")
@@ -531,7 +556,7 @@ def main(argv=None):
                              f"in turn; {secs:.1f} s), fp64 definition"}
         line = {"metric": METRIC, "value": r["value"], "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "scaling": "weak", "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
                 "config": workload_config(w, args.partials), "roofline": r["roofline"], "merge": r["merge"],
                 "cpu_baseline": cpu, "e2e": r["e2e"], "gpu_launches": r["gpu_launches"], "clocks": r["clocks"]}
         print(json.dumps(line), flush=True)

@@ -203,6 +203,24 @@ int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float 
                     const long long *cu_seqlens_q, const long long *cu_seqlens_k, int nseq, int Hq,
                     int Hkv, int D, int causal, float scale, attn_stream_t stream);
 
+/*
+ * attn_fwd_fp8 -- attention with e4m3 (FP8) Q, K, V and per-tensor scales (the
+ * FP8 attention of FlashAttention-3, page "ms-swift集成FlashAttention 2/3，
+ * 长文本训练更高效"): with q = q_scale * Q8, k = k_scale * K8, v = v_scale * V8,
+ * softmax(scale * q k^T) v and its lse, as attn_fwd. Both products run on the
+ * e4m3 tensor cores with fp32 accumulation; P is rounded to e4m3 before P V
+ * (the normaliser l is summed from the unrounded P).
+ *   q8      e4m3 [B, Hq, S, 128]; k8  e4m3 [B, Hkv, S, 128]
+ *   vt8     e4m3 [B, Hkv, 128, S]  (V transposed: keys contiguous)
+ *   o       bf16 [B, Hq, S, 128];  lse  fp32 [B, Hq, S] (natural log)
+ * Head dim 128 only and S a multiple of 16 (else ATTN_ERR_UNSUPPORTED); scales
+ * finite and positive, aligned pointers (else ATTN_ERR_INVALID_ARG). Device
+ * pointers owned by the caller; asynchronous on `stream`.
+ */
+int attn_fwd_fp8(const void *q8, const void *k8, const void *vt8, void *o, float *lse, int B, int Hq,
+                 int Hkv, int S, int D, int causal, float scale, float q_scale, float k_scale,
+                 float v_scale, attn_stream_t stream);
+
 /* Size of the library's fixed scratch array used by attn_ring_fwd_static. */
 #define SEQATTN_RING_SCRATCH_BYTES (64ull << 20) /* 64 MiB */
 

@@ -22,7 +22,7 @@ import ctypes
 
 from ._lib import AttnBlock, AttnError, lib
 
-__all__ = ["attn_fwd", "attn_partial", "attn_partial_blocks", "attn_fwd_varlen", "lse_merge",
+__all__ = ["attn_fwd", "attn_partial", "attn_partial_blocks", "attn_fwd_varlen", "attn_fwd_fp8", "lse_merge",
            "ring_attn_fwd", "ring_attn_fwd_static", "EmulatedRing",
            "query_device_error", "AttnError", "lib", "RING_SCRATCH_BYTES"]
 
@@ -186,6 +186,40 @@ def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
                              int(bool(causal)), scale, _stream_handle(q.device))
     _check(st, "attn_fwd_varlen")
     return out, lse
+
+
+def attn_fwd_fp8(q8: torch.Tensor, k8: torch.Tensor, vt8: torch.Tensor, q_scale: float, k_scale: float,
+                 v_scale: float, causal: bool = False, scale: float | None = None,
+                 out: torch.Tensor | None = None, lse: torch.Tensor | None = None):
+    """Attention on e4m3 inputs with per-tensor scales: q = q_scale*q8,
+    k = k_scale*k8, v = v_scale*vt8^T. q8 [B,Hq,S,128], k8 [B,Hkv,S,128] and the
+    transposed vt8 [B,Hkv,128,S] are contiguous torch.float8_e4m3fn CUDA
+    tensors (S a multiple of 16). Returns (O bf16 [B,Hq,S,128], lse fp32)."""
+    _require(q8.dim() == 4 and k8.dim() == 4 and vt8.dim() == 4, "expected 4-d tensors")
+    B, Hq, S, D = q8.shape
+    Hkv = k8.shape[1]
+    _require(k8.shape == (B, Hkv, S, D) and vt8.shape == (B, Hkv, D, S), "K / V^T shape mismatch")
+    for t in (q8, k8, vt8):
+        _require(t.dtype == torch.float8_e4m3fn and t.is_cuda and t.is_contiguous(),
+                 "q8, k8, vt8 must be contiguous float8_e4m3fn CUDA tensors")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty((B, Hq, S, D), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q8.device)
+    _require(out.shape == (B, Hq, S, D) and out.dtype == torch.bfloat16 and out.is_contiguous(), "bad out")
+    _require(lse.shape == (B, Hq, S) and lse.dtype == torch.float32 and lse.is_contiguous(), "bad lse")
+    st = lib.attn_fwd_fp8(q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(), out.data_ptr(), lse.data_ptr(), B, Hq,
+                          Hkv, S, D, int(bool(causal)), scale, float(q_scale), float(k_scale), float(v_scale),
+                          _stream_handle(q8.device))
+    _check(st, "attn_fwd_fp8")
+    return out, lse
+
+
+def quantize_e4m3(x: torch.Tensor, scale: float) -> torch.Tensor:
+    """x / scale rounded to e4m3 (nearest even, clamped to +-448): input
+    preparation for attn_fwd_fp8 (torch's conversion)."""
+    return (x.float() / scale).clamp_(-448.0, 448.0).to(torch.float8_e4m3fn)
 
 
 def lse_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, out_dtype=torch.bfloat16,

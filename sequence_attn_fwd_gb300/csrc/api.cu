@@ -82,6 +82,22 @@ bool make_out_map(CUtensorMap *map, void *base, int D, long long rows, long long
 
 bool scale_ok(float scale) { return isfinite(scale) && scale > 0.f; }
 
+// 3-D byte view [heads][rows][cols] of e4m3 data (rows contiguous), box
+// 128 x 128 x 1 with 128-byte swizzle.
+bool make_map_u8(CUtensorMap *map, const void *base, long long cols, long long rows, long long heads) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols),
+                           static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(cols)};
+  cuuint32_t box[3] = {128u, 128u, 1u};
+  cuuint32_t estride[3] = {1u, 1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box,
+            estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 constexpr long long kMaxRowsPerHead = 1ll << 30;  // keeps every row index within int range
 
 int run_attention(const void *q, const void *k, const void *v, long long q_off, long long kv_off,
@@ -131,6 +147,7 @@ int run_attention(const void *q, const void *k, const void *v, long long q_off, 
   p.n_qblocks = (Sq + 255) / 256;
   p.skip_empty = skip_empty ? 1 : 0;
   p.o_rows = Sq;
+  p.o_scale = 1.f;
   cudaError_t e = seqattn::launch_attention(D, f32_out, pair, tq, tk, tv, to, p, stream);
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
@@ -161,6 +178,7 @@ int run_blocks(const void *q, const void *k, const void *v, void *o, float *lse,
   p.causal = causal;
   p.skip_empty = skip_empty ? 1 : 0;
   p.o_rows = o_rows;
+  p.o_scale = 1.f;
   for (size_t first = 0; first < blocks.size(); first += seqattn::kMaxLaunchBlocks) {
     seqattn::BlockTable tbl{};
     const size_t n = std::min(blocks.size() - first, static_cast<size_t>(seqattn::kMaxLaunchBlocks));
@@ -220,6 +238,47 @@ int check_common(const void *q, const void *k, const void *v, const void *o, con
 }  // namespace
 
 extern "C" {
+
+int attn_fwd_fp8(const void *q8, const void *k8, const void *vt8, void *o, float *lse, int B, int Hq,
+                 int Hkv, int S, int D, int causal, float scale, float q_scale, float k_scale,
+                 float v_scale, attn_stream_t stream) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || S < 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (!scale_ok(scale) || !scale_ok(q_scale) || !scale_ok(k_scale) || !scale_ok(v_scale))
+    return ATTN_ERR_INVALID_ARG;
+  if (D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (S % 16 != 0) return ATTN_ERR_UNSUPPORTED;  // V^T rows of S bytes must be 16-byte multiples
+  if (S > kMaxRowsPerHead || (S + 255ll) / 256 > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Hq > 0x7fffffffll) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || S == 0) return ATTN_OK;
+  if (!q8 || !k8 || !vt8 || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(vt8) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return ATTN_ERR_INVALID_ARG;
+  CUtensorMap tq, tk, tvt, to;
+  const long long heads = static_cast<long long>(B) * Hq, kv_heads = static_cast<long long>(B) * Hkv;
+  if (!make_map_u8(&tq, q8, D, S, heads) || !make_map_u8(&tk, k8, D, S, kv_heads) ||
+      !make_map_u8(&tvt, vt8, S, D, kv_heads) || !make_out_map(&to, o, D, S, heads, false))
+    return cuda_fail(cudaErrorInvalidValue);
+  seqattn::AttnParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Sq = S;
+  p.Skv = S;
+  p.q_off = 0;
+  p.kv_off = 0;
+  p.scale_log2 = scale * q_scale * k_scale * 1.4426950408889634f;
+  p.causal = causal;
+  p.n_qblocks = (S + 255) / 256;
+  p.skip_empty = 0;
+  p.o_rows = S;
+  p.o_scale = v_scale;
+  cudaError_t e = seqattn::launch_attention_fp8(tq, tk, tvt, to, p, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
 
 int attn_partial_blocks(const void *q, const void *k, const void *v, float *o_part, float *lse_part,
                         const attn_block *blocks, int n_blocks, int B, int Hq, int Hkv,

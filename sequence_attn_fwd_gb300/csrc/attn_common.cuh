@@ -100,9 +100,10 @@ __device__ __forceinline__ uint64_t exp2_pair(uint64_t x, bool poly) {
 }
 
 // P = 2^(s * c2 - m_ref) for the 128 scores of a row, packed as bf16 pairs
-// (element 2i in the low half), returning the fp32 sum of the unrounded P.
-// With kTrackMax the raw row maximum is found in the same pass.
-template <bool kTrackMax>
+// (element 2i in the low half) or, with kFp8, as e4m3 quads, returning the
+// fp32 sum of the unrounded P. With kTrackMax the raw row maximum is found in
+// the same pass.
+template <bool kTrackMax, bool kFp8 = false>
 __device__ __forceinline__ float exp_row(const float *s, float c2, float m_ref, uint32_t *pk,
                                          float *mx_out) {
   const uint64_t scale2 = f2_pack(c2, c2);
@@ -124,10 +125,14 @@ __device__ __forceinline__ float exp_row(const float *s, float c2, float m_ref, 
     float p0, p1, p2, p3;
     f2_unpack(pa, p0, p1);
     f2_unpack(pb, p2, p3);
-    __nv_bfloat162 h0 = __floats2bfloat162_rn(p0, p1);
-    __nv_bfloat162 h1 = __floats2bfloat162_rn(p2, p3);
-    pk[q] = *reinterpret_cast<uint32_t *>(&h0);
-    pk[q + 1] = *reinterpret_cast<uint32_t *>(&h1);
+    if constexpr (kFp8) {  // four e4m3 per 32-bit TMEM column, element 4i in the low byte
+      pk[q / 2] = pack_e4m3x2(p0, p1) | (pack_e4m3x2(p2, p3) << 16);
+    } else {
+      __nv_bfloat162 h0 = __floats2bfloat162_rn(p0, p1);
+      __nv_bfloat162 h1 = __floats2bfloat162_rn(p2, p3);
+      pk[q] = *reinterpret_cast<uint32_t *>(&h0);
+      pk[q + 1] = *reinterpret_cast<uint32_t *>(&h1);
+    }
   }
   if (kTrackMax) *mx_out = fmaxf(ma, mb);
   float a0, a1, b0, b1;
@@ -178,7 +183,7 @@ struct EpilogueStore {
 //                     that works through several tiles keeps counting)
 //   ofull_parity      parity of the bar_ofull phase that marks this tile's O
 // Returns false if the pipeline was aborted.
-template <int D, bool kF32Out, typename SignalP>
+template <int D, bool kF32Out, typename SignalP, bool kFp8 = false>
 __device__ __forceinline__ bool softmax_row(const AttnParams &p, const BlockDesc &blk, int row,
                                             int tile_first_row, int n,
                                             uint32_t s_addr, uint32_t o_addr, uint32_t bar_sfull,
@@ -232,13 +237,13 @@ __device__ __forceinline__ bool softmax_row(const AttnParams &p, const BlockDesc
         if (j == 0) {
           // no reference yet: the tile maximum first, then the exponentials
           m = row_max(s) * c2;
-          rowsum = exp_row<false>(s, c2, (m == -INFINITY) ? 0.f : m, pk, nullptr);
+          rowsum = exp_row<false, kFp8>(s, c2, (m == -INFINITY) ? 0.f : m, pk, nullptr);
         } else {
           // Exponentiate against the current reference while finding the tile
           // maximum; only if some row's maximum grew by more than 2^8 (rare
           // after the first tiles) is O rescaled and the pass redone.
           float mx;
-          rowsum = exp_row<true>(s, c2, (m == -INFINITY) ? 0.f : m, pk, &mx);
+          rowsum = exp_row<true, kFp8>(s, c2, (m == -INFINITY) ? 0.f : m, pk, &mx);
           m_grow = fmaxf(m, mx * c2);
         }
       }
@@ -264,13 +269,13 @@ __device__ __forceinline__ bool softmax_row(const AttnParams &p, const BlockDesc
           tmem_st_wait();
           uint32_t sr[128];
           load_scores(sr);
-          rowsum = exp_row<false>(reinterpret_cast<const float *>(sr), c2,
-                                  (m == -INFINITY) ? 0.f : m, pk, nullptr);
+          rowsum = exp_row<false, kFp8>(reinterpret_cast<const float *>(sr), c2,
+                                        (m == -INFINITY) ? 0.f : m, pk, nullptr);
         }
       }
       l += rowsum;
       tmem_st32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_st32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      if constexpr (!kFp8) tmem_st32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
       tmem_st_wait();
       tc_fence_before();
       signal_p();
@@ -284,7 +289,8 @@ __device__ __forceinline__ bool softmax_row(const AttnParams &p, const BlockDesc
     }
     const bool row_valid = row < blk.Sq;
     const bool write_o = row_valid && !(p.skip_empty && l == 0.f);
-    const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+    float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+    if constexpr (kFp8) inv_l *= p.o_scale;  // dequantisation of V
     bool via_tma = store.map != nullptr;
     if (via_tma) {
       // Whole-box stores need the final O on every row, no row that must stay

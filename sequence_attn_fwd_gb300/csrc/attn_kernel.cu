@@ -50,11 +50,13 @@ constexpr int kThreads = 320;
 constexpr int kMmaWarp = 8;
 constexpr int kTmaWarp = 9;
 
-template <int D>
+template <int D, bool kFp8 = false>
 struct Cfg {
-  static constexpr int kColBlocks = D / 64;
-  static constexpr int kTileBytes = kRowsPerTile * D * 2;
-  static constexpr int kStages = (D == 128) ? 4 : 8;
+  static constexpr int kElemBytes = kFp8 ? 1 : 2;              // bf16 or e4m3 operands
+  static constexpr int kColBlocks = D * kElemBytes / 128;        // 128-byte column blocks of a row
+  static constexpr int kColBlockElems = 128 / kElemBytes;
+  static constexpr int kTileBytes = kRowsPerTile * D * kElemBytes;
+  static constexpr int kStages = 131072 / kTileBytes;            // a 128 KB K/V ring
   static constexpr int kSmemQ = 2 * kTileBytes;
   static constexpr int kSmemRing = kStages * kTileBytes;
   static constexpr int kStageBytes = 16384;  // epilogue staging box of one softmax warpgroup
@@ -64,7 +66,8 @@ struct Cfg {
   static constexpr int kSmemBytes =
       1024 + kSmemQ + kSmemRing + kSmemStage + 8 * kNumBarriers + 16;
 };
-static_assert(Cfg<128>::kSmemBytes <= 232448 && Cfg<64>::kSmemBytes <= 232448,
+static_assert(Cfg<128>::kSmemBytes <= 232448 && Cfg<64>::kSmemBytes <= 232448 &&
+                  Cfg<128, true>::kSmemBytes <= 232448,
               "shared memory per CTA");
 
 // Work item k of a launch: 256 query rows of one (batch, head) of one block of
@@ -120,14 +123,17 @@ __device__ __forceinline__ Item item_of(const AttnParams &p, const BlockTable &t
   return {lo, static_cast<int>(local % heads), qblock * 2 * kRowsPerTile};
 }
 
-template <int D, bool kF32Out, typename Table>
+// kFp8: Q, K in e4m3 with K-major tiles, V given transposed ([heads][D][keys],
+// so its tiles are K-major too), P rounded to e4m3 in TMEM (one instantiation:
+// D = 128, bf16 output, single problem).
+template <int D, bool kF32Out, typename Table, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_o, const AttnParams p,
                     const __grid_constant__ Table tbl) {
-  using C = Cfg<D>;
+  using C = Cfg<D, kFp8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -212,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t)
           for (int cb = 0; cb < C::kColBlocks; ++cb)
             tma_load_3d(smem_addr(sQ + (t * C::kColBlocks + cb) * kColBlockBytes), &tm_q,
-                        bar(kBarQFull), cb * 64, q_row + t * kRowsPerTile, it.bh);
+                        bar(kBarQFull), cb * C::kColBlockElems, q_row + t * kRowsPerTile, it.bh);
         ++nq;
         const int b = it.bh / p.Hq, hq = it.bh % p.Hq;
         const int kv_head = b * p.Hkv + hq / (p.Hq / p.Hkv);
@@ -225,10 +231,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             mbar_arrive_expect_tx(bar(kBarFull + slot), C::kTileBytes);
-            const CUtensorMap *map = which ? &tm_v : &tm_k;
-            for (int cb = 0; cb < C::kColBlocks; ++cb)
-              tma_load_3d(smem_addr(sRing + (slot * C::kColBlocks + cb) * kColBlockBytes), map,
-                          bar(kBarFull + slot), cb * 64, kv_row + j * kRowsPerTile, kv_head);
+            if (kFp8 && which) {
+              // V^T tile j: the 128 keys of the tile along x, all D rows (one box at D = 128)
+              tma_load_3d(smem_addr(sRing + slot * C::kTileBytes), &tm_v, bar(kBarFull + slot),
+                          kv_row + j * kRowsPerTile, 0, kv_head);
+            } else {
+              const CUtensorMap *map = which ? &tm_v : &tm_k;
+              for (int cb = 0; cb < C::kColBlocks; ++cb)
+                tma_load_3d(smem_addr(sRing + (slot * C::kColBlocks + cb) * kColBlockBytes), map,
+                            bar(kBarFull + slot), cb * C::kColBlockElems, kv_row + j * kRowsPerTile,
+                            kv_head);
+            }
           }
         }
       }
@@ -242,8 +255,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && !skip) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, true);
+      constexpr uint32_t idesc_s = kFp8 ? idesc_e4m3_f32(128, 128) : idesc_bf16_f32(128, 128, false);
+      constexpr uint32_t idesc_o = kFp8 ? idesc_e4m3_f32(128, D) : idesc_bf16_f32(128, D, true);
+      constexpr int kKSteps = D * C::kElemBytes / 32;  // 32-byte K steps of S = Q K^T
       const uint32_t q_base = smem_addr(sQ);
       const uint32_t ring_base = smem_addr(sRing);
       int c = 0;             // ring position of the item's K_0
@@ -285,10 +299,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
               }
               tc_fence_after();
+              if constexpr (kFp8) {
+                // B = V^T tile, K-major: 32 keys (32 bytes) per step; A = 8 TMEM columns of P
 #pragma unroll
-              for (int kk = 0; kk < kRowsPerTile / 16; ++kk) {
-                const uint64_t bdesc = sw128_desc(v_base + kk * 2048, kColBlockBytes, 1024);
-                mma_ts(tO(t), tS(t) + kk * 8, bdesc, idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < kRowsPerTile / 32; ++kk)
+                  mma_ts_e4m3(tO(t), tS(t) + kk * 8, sw128_desc(v_base + kk * 32, 16, 1024), idesc_o,
+                              (j > 1 || kk > 0) ? 1u : 0u);
+              } else {
+#pragma unroll
+                for (int kk = 0; kk < kRowsPerTile / 16; ++kk) {
+                  const uint64_t bdesc = sw128_desc(v_base + kk * 2048, kColBlockBytes, 1024);
+                  mma_ts(tO(t), tS(t) + kk * 8, bdesc, idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
+                }
               }
               if (j - 1 == nt - 1) mma_commit(bar(kBarOFull + t));
               if (t == 1 || j - 1 >= n_t[1]) mma_commit(bar(kBarEmpty + sV));  // last use of V_{j-1}
@@ -297,10 +319,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               // S_t = Q_t K_j^T
               const uint32_t qt = q_base + t * C::kTileBytes;
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
+              for (int kk = 0; kk < kKSteps; ++kk) {
                 const uint32_t off = (kk / 4) * kColBlockBytes + (kk % 4) * 32;
-                mma_ss(tS(t), sw128_desc(qt + off, 16, 1024), sw128_desc(k_base + off, 16, 1024),
-                       idesc_s, kk > 0 ? 1u : 0u);
+                if constexpr (kFp8)
+                  mma_ss_e4m3(tS(t), sw128_desc(qt + off, 16, 1024), sw128_desc(k_base + off, 16, 1024),
+                              idesc_s, kk > 0 ? 1u : 0u);
+                else
+                  mma_ss(tS(t), sw128_desc(qt + off, 16, 1024), sw128_desc(k_base + off, 16, 1024),
+                         idesc_s, kk > 0 ? 1u : 0u);
               }
               mma_commit(bar(kBarSFull + t));
               if (t == 1 || j >= n_t[1]) mma_commit(bar(kBarEmpty + sK));  // last use of K_j
@@ -340,14 +366,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int row = tile_first + row_in_tile;
       const EpilogueStore store{&tm_o, stage, 1 + t, out_head};
-      const bool ok = softmax_row<D, kF32Out>(
+      auto signal_p = [&] {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pfull);  // one arrival per warp
+      };
+      const bool ok = softmax_row<D, kF32Out, decltype(signal_p), kFp8>(
           p, blk, row, tile_first, n, tS(t) + lane_off, tO(t) + lane_off, bar(kBarSFull + t),
           bar(kBarOFull + t), g, u & 1u,
           static_cast<size_t>(out_head) * p.o_rows + static_cast<size_t>(blk.o_row + row),
-          abort_flag, err, store, [&] {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(pfull);  // one arrival per warp
-          });
+          abort_flag, err, store, signal_p);
       g += n;
       ++u;
       if (!ok) break;  // the same on every thread of the warpgroup
@@ -378,19 +405,18 @@ int sm_count() {
   return n;
 }
 
-template <int D, bool kF32Out, typename Table>
+template <int D, bool kF32Out, typename Table, bool kFp8 = false>
 cudaError_t launch_typed(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                          const CUtensorMap &to, const AttnParams &p, const Table &tbl,
                          long long n_items, cudaStream_t stream) {
-  auto kernel = attn_fwd_kernel<D, kF32Out, Table>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Cfg<D>::kSmemBytes);
+  auto kernel = attn_fwd_kernel<D, kF32Out, Table, kFp8>;
+  constexpr int kSmem = Cfg<D, kFp8>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   if (n_items == 0) return cudaSuccess;
   // persistent: one CTA per SM (or per work item, if there are fewer)
   const long long grid = n_items < sm_count() ? n_items : sm_count();
-  kernel<<<static_cast<unsigned>(grid), kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, to, p,
-                                                                               tbl);
+  kernel<<<static_cast<unsigned>(grid), kThreads, kSmem, stream>>>(tq, tk, tv, to, p, tbl);
   return cudaGetLastError();
 }
 
@@ -429,6 +455,13 @@ cudaError_t launch_attention(int D, bool f32_out, bool pair, const CUtensorMap &
                            : pair2sm::launch_pair<false>(tq, tk, tv, p, stream);
   return launch_dispatch(D, f32_out, tq, tk, tv, to, p, SingleProblem{0},
                          static_cast<long long>(p.B) * p.Hq * p.n_qblocks, stream);
+}
+
+cudaError_t launch_attention_fp8(const CUtensorMap &tq, const CUtensorMap &tk,
+                                 const CUtensorMap &tvt, const CUtensorMap &to,
+                                 const AttnParams &p, cudaStream_t stream) {
+  return launch_typed<128, false, SingleProblem, true>(
+      tq, tk, tvt, to, p, SingleProblem{0}, static_cast<long long>(p.B) * p.Hq * p.n_qblocks, stream);
 }
 
 cudaError_t launch_attention_blocks(int D, bool f32_out, const CUtensorMap &tq,

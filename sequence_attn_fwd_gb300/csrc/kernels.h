@@ -18,6 +18,7 @@ struct AttnParams {
   int n_qblocks;      // ceil(Sq / 256): two 128-row query tiles per CTA
   int skip_empty;     // rows that see no key: write lse = -inf only, leave O untouched
   long long o_rows;   // rows per head of O and lse (Sq for a single problem)
+  float o_scale;      // e4m3 attention: the V scale applied to O (1 otherwise)
 };
 
 // One block of attention: the queries in rows [q_row, q_row + Sq) of Q (per
@@ -53,6 +54,14 @@ bool attention_uses_pair(int D);
 cudaError_t launch_attention(int D, bool f32_out, bool pair, const CUtensorMap &tm_q,
                              const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                              const CUtensorMap &tm_o, const AttnParams &p, cudaStream_t stream);
+
+// e4m3 attention (D = 128, bf16 O): tq / tk over e4m3 [heads][S][128] with
+// box 128 x 128 x 1, tvt over V^T e4m3 [kv heads][128][S] with box 128 (keys)
+// x 128 x 1, all 128-byte swizzle; p.scale_log2 includes the Q and K scales,
+// p.o_scale is the V scale.
+cudaError_t launch_attention_fp8(const CUtensorMap &tq, const CUtensorMap &tk,
+                                 const CUtensorMap &tvt, const CUtensorMap &to,
+                                 const AttnParams &p, cudaStream_t stream);
 
 // The single-SM persistent kernel over a table of blocks (row ranges of the
 // maps' row dimension; p's Sq / Skv / q_off / kv_off / n_qblocks are unused).

@@ -32,7 +32,8 @@ def test_header_declares_the_boundary():
     assert declared_functions() == sorted(["attn_fwd", "attn_partial", "lse_merge", "attn_query_device_error",
                                            "attn_status_string", "attn_last_cuda_error",
                                            "attn_ring_fwd_static", "attn_debug_expire_wait",
-                                           "attn_debug_exp2", "attn_partial_blocks", "attn_fwd_varlen"])
+                                           "attn_debug_exp2", "attn_partial_blocks", "attn_fwd_varlen",
+                                           "attn_fwd_fp8"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -157,3 +158,15 @@ def test_attn_fwd_varlen_argument_checks(lib):
     assert run([0, 5, 3], [0, 5, 9]) == 1  # decreasing
     assert run([0, 5], [0, 5], Hq=3, Hkv=2) == 1
     assert run([0, 5], [0, 5], D=32) == 2
+
+
+def test_attn_fwd_fp8_argument_checks(lib):
+    def run(S=256, D=128, Hq=2, Hkv=1, qs=1.0, vs=1.0, causal=1):
+        return lib.attn_fwd_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, 1, Hq, Hkv, S, D, causal, ctypes.c_float(0.1),
+                                ctypes.c_float(qs), ctypes.c_float(1.0), ctypes.c_float(vs), None)
+
+    assert run(D=64) == 2
+    assert run(S=100) == 2  # V^T rows must be 16-byte multiples
+    assert run(qs=0.0) == 1 and run(vs=float("inf")) == 1
+    assert run(Hq=3, Hkv=2) == 1 and run(causal=3) == 1
+    assert run(S=0) == 0

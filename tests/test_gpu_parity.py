@@ -4,6 +4,8 @@ Small cases span several 128-row tiles and a ragged tail and are checked in
 full; the five named workloads run at full size in the launch configuration
 the benchmark times and are checked on sampled query rows.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -300,6 +302,58 @@ def test_ring_grouped_launch_is_bitwise_the_per_chunk_launches(sa):
     o2, l2 = sa.ring_attn_fwd(q, k, v, P=4, causal=True, grouped=True)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def fp8_bound(qd, kd, vd, causal, scale):
+    """Per-element bound on |O_fp8 - O_exact| for inputs already on the e4m3
+    grid (numpy fp64, small shapes): P is rounded to e4m3 in the kernel, so
+    |dP| <= 2^-4 P (normal range) or 2^-10 (below 2^-6) in units where the row
+    maximum is >= 1 (the kernel's reference maximum never exceeds the true one),
+    and |dO_d| <= (2^-4 sum_j P_j |v_jd| + 2^-10 sum_{P_j < 2^-6} |v_jd|) / l;
+    plus the bf16 rounding of O."""
+    q, k, v = (t.double().numpy() for t in (qd, kd, vd))
+    B, Hq, S, D = q.shape
+    g = Hq // k.shape[1]
+    bound = np.empty((B, Hq, S, D))
+    for b in range(B):
+        for h in range(Hq):
+            s = scale * q[b, h] @ k[b, h // g].T
+            if causal:
+                s = np.where(np.tril(np.ones((S, S), dtype=bool)), s, -np.inf)
+            p = np.exp(s - s.max(axis=1, keepdims=True))
+            l = p.sum(axis=1, keepdims=True)
+            av = np.abs(v[b, h // g])
+            bound[b, h] = (2.0 ** -4 * (p @ av) + 2.0 ** -10 * ((p < 2.0 ** -6) @ av)) / l
+    return bound
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 2, 512, True), (1, 4, 2, 1008, True), (2, 2, 1, 384, False)],
+                         ids=["s512c", "gqa_s1008c", "b2_s384"])
+def test_attn_fwd_fp8_against_oracle(sa, shape):
+    """e4m3 Q, K, V with power-of-two scales (so the dequantised inputs are exact
+    bf16 and the oracle computes the exact attention of the quantised data);
+    the kernel's only error beyond rounding is P in e4m3, held to the bound
+    derived in fp8_bound plus 2^-8 |O| + 1e-4."""
+    B, Hq, Hkv, S, causal = shape
+    D = 128
+    q, k, v = workloads.make_qkv(adhoc(B, Hq, Hkv, S, D, causal, seed=61))
+    qs, ks, vs = 0.25, 0.5, 0.25
+    q8, k8, v8 = (sa.quantize_e4m3(t, sc) for t, sc in ((q, qs), (k, ks), (v, vs)))
+    qd, kd, vd = ((t.float() * sc).to(torch.bfloat16) for t, sc in ((q8, qs), (k8, ks), (v8, vs)))
+    assert torch.equal(qd.float(), q8.float() * qs)  # exact: the dequantised inputs are bf16 values
+    o_ref, lse_ref = oracle.attention(qd, kd, vd, causal)
+    vt8 = v8.transpose(2, 3).contiguous()
+    o, lse = sa.attn_fwd_fp8(q8.cuda(), k8.cuda(), vt8.cuda(), qs, ks, vs, causal=causal)
+    torch.cuda.synchronize()
+    check_lse(lse, lse_ref)
+    err = np.abs(o.double().cpu().numpy() - o_ref)
+    bound = fp8_bound(qd, kd, vd, causal, 1.0 / math.sqrt(D)) + 2.0 ** -8 * np.abs(o_ref) + 1e-4
+    assert np.isfinite(o.float().cpu().numpy()).all()
+    worst = float((err / bound).max())
+    assert worst <= 1.0, f"fp8 error exceeds its bound by {worst:.2f}x"
+    # rounding errors of many P elements partly cancel: the mean error sits well
+    # below the mean of the worst-case bound (a layout or scale mistake would not)
+    assert float(err.mean()) <= 0.25 * float(bound.mean())
 
 
 # ----------------------------------------------------------------- full-size workloads

@@ -91,6 +91,12 @@ __device__ __forceinline__ uint64_t exp2_poly_x2(uint64_t x) {
 #define SEQATTN_POLY_EXP_PAIRS_PER_8 2
 #endif
 constexpr int kPolyExpPairsPer8 = SEQATTN_POLY_EXP_PAIRS_PER_8;
+// The e4m3 kernel measured fastest with every exponential on the MUFU (its
+// softmax is bound by instruction issue, which the polynomial adds to).
+#ifndef SEQATTN_POLY_EXP_PAIRS_PER_8_FP8
+#define SEQATTN_POLY_EXP_PAIRS_PER_8_FP8 0
+#endif
+constexpr int kPolyExpPairsPer8Fp8 = SEQATTN_POLY_EXP_PAIRS_PER_8_FP8;
 
 __device__ __forceinline__ uint64_t exp2_pair(uint64_t x, bool poly) {
   if (poly) return exp2_poly_x2(x);
@@ -112,10 +118,11 @@ __device__ __forceinline__ float exp_row(const float *s, float c2, float m_ref, 
   float ma = -INFINITY, mb = -INFINITY;
 #pragma unroll
   for (int q = 0; q < 64; q += 2) {  // pairs q and q + 1: elements 2q .. 2q + 3
+    constexpr int kPoly = kFp8 ? kPolyExpPairsPer8Fp8 : kPolyExpPairsPer8;
     const uint64_t pa = exp2_pair(f2_fma(f2_pack(s[2 * q], s[2 * q + 1]), scale2, neg_m2),
-                                  (q % 8) < kPolyExpPairsPer8);
+                                  (q % 8) < kPoly);
     const uint64_t pb = exp2_pair(f2_fma(f2_pack(s[2 * q + 2], s[2 * q + 3]), scale2, neg_m2),
-                                  ((q + 1) % 8) < kPolyExpPairsPer8);
+                                  ((q + 1) % 8) < kPoly);
     sum_a = f2_add(sum_a, pa);
     sum_b = f2_add(sum_b, pb);
     if (kTrackMax) {

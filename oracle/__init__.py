@@ -11,6 +11,9 @@ attention(q, k, v, causal, scale=None, q_off=0, kv_off=0, rows=None, threads=Non
     See attn_oracle.c for the definition and the passages it follows.
 lse_merge(o_parts, lse_parts)
     fp64 merge of per-chunk partials ([P,...,D], [P,...]).
+attention_backward(q, k, v, dout, causal, scale=None, threads=None)
+    fp64 gradients (dQ, dK, dV) of attention for the output gradient dO
+    (bf16 [B,Hq,S,D]); see attn_oracle.c.
 """
 from __future__ import annotations
 
@@ -50,6 +53,9 @@ def _load():
         lib.oracle_attention.restype = ctypes.c_int
         lib.oracle_lse_merge.argtypes = [P, P, ctypes.c_int, ctypes.c_longlong, ctypes.c_int, P, P]
         lib.oracle_lse_merge.restype = None
+        lib.oracle_attention_backward.argtypes = [P, P, P, P] + [ctypes.c_int] * 6 + [
+            ctypes.c_double, P, P, P, ctypes.c_int]
+        lib.oracle_attention_backward.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -107,3 +113,24 @@ def lse_merge(o_parts, lse_parts):
     _load().oracle_lse_merge(o_parts.ctypes.data, lse_parts.ctypes.data, P, nrows, D,
                              o.ctypes.data, lse.ctypes.data)
     return o, lse
+
+
+def attention_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dout: torch.Tensor, causal: bool,
+                       scale: float | None = None, threads: int | None = None):
+    """fp64 (dQ [B,Hq,S,D], dK [B,Hkv,S,D], dV [B,Hkv,S,D]) as numpy from bf16
+    q, dout [B,Hq,S,D] and k, v [B,Hkv,S,D] (the chain rule through the
+    definition; attn_oracle.c)."""
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    assert k.shape == (B, Hkv, S, D) and v.shape == k.shape and dout.shape == q.shape and Hq % Hkv == 0
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    qb, kb, vb, db = _bits(q), _bits(k), _bits(v), _bits(dout)
+    dq = np.empty((B, Hq, S, D), dtype=np.float64)
+    dk = np.empty((B, Hkv, S, D), dtype=np.float64)
+    dv = np.empty((B, Hkv, S, D), dtype=np.float64)
+    rc = _load().oracle_attention_backward(qb.ctypes.data, kb.ctypes.data, vb.ctypes.data, db.ctypes.data,
+                                           B, Hq, Hkv, S, D, int(bool(causal)), scale, dq.ctypes.data,
+                                           dk.ctypes.data, dv.ctypes.data, int(threads or default_threads()))
+    if rc != 0:
+        raise ValueError("oracle_attention_backward rejected its arguments")
+    return dq, dk, dv

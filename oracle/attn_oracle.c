@@ -231,3 +231,123 @@ void oracle_lse_merge(const double *o_parts, const double *lse_parts, int P, lon
         lse[r] = M + log(wsum);
     }
 }
+
+/*
+ * Backward of attention: the gradients of Q, K and V for a loss whose
+ * gradient with respect to O is dO. The pages mention the backward pass that
+ * FlashAttention recomputes block by block (page "ms-swift集成FlashAttention
+ * 2/3，长文本训练更高效", section "FlashAttention 如何破局？不只是融合内核")
+ * without writing it out; this is the chain rule through the definition above
+ * (visibility and GQA mapping as there, q_off = kv_off = 0, Sq = Skv = S):
+ *   P_ij  = exp(s_ij - m_i) / l_i                 (the softmax of row i)
+ *   dV_j  = sum_i P_ij dO_i
+ *   dP_ij = <dO_i, v_j>
+ *   dS_ij = P_ij (dP_ij - sum_t P_it dP_it)        (the softmax Jacobian)
+ *   dQ_i  = scale * sum_j dS_ij k_j
+ *   dK_j  = scale * sum_i dS_ij q_i
+ * dK and dV of a KV head sum over the query heads of its group.
+ */
+typedef struct {
+    const uint16_t *q, *k, *v, *dout;
+    int B, Hq, Hkv, S, D, causal;
+    double scale;
+    double *dq, *dk, *dv;
+    int nthreads, tid;
+} bwd_job;
+
+static void *backward_worker(void *arg)
+{
+    const bwd_job *j = (const bwd_job *)arg;
+    const int S = j->S, D = j->D, group = j->Hq / j->Hkv;
+    double *p = (double *)malloc(sizeof(double) * (size_t)(S > 0 ? S : 1));
+    double *dp = (double *)malloc(sizeof(double) * (size_t)(S > 0 ? S : 1));
+    if (!p || !dp) {
+        free(p);
+        free(dp);
+        return (void *)1;
+    }
+    /* one (batch, KV head) per item: its dK, dV and its query heads' dQ */
+    for (int item = j->tid; item < j->B * j->Hkv; item += j->nthreads) {
+        const int b = item / j->Hkv, hkv = item % j->Hkv;
+        const uint16_t *kh = j->k + ((long long)b * j->Hkv + hkv) * S * D;
+        const uint16_t *vh = j->v + ((long long)b * j->Hkv + hkv) * S * D;
+        double *dkh = j->dk + ((long long)b * j->Hkv + hkv) * S * D;
+        double *dvh = j->dv + ((long long)b * j->Hkv + hkv) * S * D;
+        for (long long t = 0; t < (long long)S * D; t++) dkh[t] = dvh[t] = 0.0;
+        for (int hq = hkv * group; hq < (hkv + 1) * group; hq++) {
+            const uint16_t *qh = j->q + ((long long)b * j->Hq + hq) * S * D;
+            const uint16_t *doh = j->dout + ((long long)b * j->Hq + hq) * S * D;
+            double *dqh = j->dq + ((long long)b * j->Hq + hq) * S * D;
+            for (long long i = 0; i < S; i++) {
+                const long long nvis = j->causal ? i + 1 : S;
+                const uint16_t *qi = qh + i * D, *doi = doh + i * D;
+                double *dqi = dqh + i * D;
+                for (int d = 0; d < D; d++) dqi[d] = 0.0;
+                /* the row's softmax */
+                double m = -INFINITY;
+                for (long long t = 0; t < nvis; t++) {
+                    double dot = 0.0;
+                    for (int d = 0; d < D; d++) dot += bf16_to_double(qi[d]) * bf16_to_double(kh[t * D + d]);
+                    p[t] = j->scale * dot;
+                    if (p[t] > m) m = p[t];
+                }
+                double l = 0.0;
+                for (long long t = 0; t < nvis; t++) {
+                    p[t] = exp(p[t] - m);
+                    l += p[t];
+                }
+                for (long long t = 0; t < nvis; t++) p[t] /= l;
+                /* dP and its P-weighted row sum */
+                double psum = 0.0;
+                for (long long t = 0; t < nvis; t++) {
+                    double dot = 0.0;
+                    for (int d = 0; d < D; d++) dot += bf16_to_double(doi[d]) * bf16_to_double(vh[t * D + d]);
+                    dp[t] = dot;
+                    psum += p[t] * dot;
+                }
+                for (long long t = 0; t < nvis; t++) {
+                    const double ds = p[t] * (dp[t] - psum);
+                    for (int d = 0; d < D; d++) {
+                        dqi[d] += j->scale * ds * bf16_to_double(kh[t * D + d]);
+                        dkh[t * D + d] += j->scale * ds * bf16_to_double(qi[d]);
+                        dvh[t * D + d] += p[t] * bf16_to_double(doi[d]);
+                    }
+                }
+            }
+        }
+    }
+    free(p);
+    free(dp);
+    return NULL;
+}
+
+/*
+ * q, k, v, dout: bf16 bits, contiguous [B][H][S][D]; dq [B][Hq][S][D], dk and
+ * dv [B][Hkv][S][D] doubles (outputs). Returns 0, or -1 on invalid arguments.
+ */
+int oracle_attention_backward(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                              const uint16_t *dout, int B, int Hq, int Hkv, int S, int D,
+                              int causal, double scale, double *dq, double *dk, double *dv,
+                              int nthreads)
+{
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || S < 0 || D <= 0) return -1;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    pthread_t th[256];
+    bwd_job jobs[256];
+    int rc = 0;
+    for (int t = 0; t < nthreads; t++) {
+        jobs[t] = (bwd_job){q, k, v, dout, B, Hq, Hkv, S, D, causal, scale, dq, dk, dv, nthreads, t};
+        if (pthread_create(&th[t], NULL, backward_worker, &jobs[t]) != 0) {
+            nthreads = t;
+            rc = -1;
+            break;
+        }
+    }
+    for (int t = 0; t < nthreads; t++) {
+        void *ret = NULL;
+        pthread_join(th[t], &ret);
+        if (ret) rc = -1;
+    }
+    return rc;
+}

@@ -221,6 +221,26 @@ int attn_fwd_fp8(const void *q8, const void *k8, const void *vt8, void *o, float
                  int Hkv, int S, int D, int causal, float scale, float q_scale, float k_scale,
                  float v_scale, attn_stream_t stream);
 
+/*
+ * attn_bwd -- gradients of attention (dQ, dK, dV) for the output gradient dO,
+ * recomputing the scores tile by tile from Q, K and the forward's lse (the
+ * backward FlashAttention recomputes block by block, page "ms-swift集成
+ * FlashAttention 2/3，长文本训练更高效"):
+ *   P = exp(scale Q K^T - lse),  delta_i = <dO_i, O_i>,
+ *   dV = P^T dO,  dS = P * (dO V^T - delta),  dK = scale dS^T Q,  dQ = scale dS K,
+ * dK and dV summed over the query heads of each GQA group.
+ *   q, o, dout  bf16 [B, Hq, S, 128];  k, v  bf16 [B, Hkv, S, 128]
+ *   lse         fp32 [B, Hq, S] from attn_fwd (natural log)
+ *   delta       fp32 [B, Hq, S] workspace (written, then read)
+ *   dq          bf16 [B, Hq, S, 128];  dk, dv  bf16 [B, Hkv, S, 128]  (outputs)
+ * Head dim 128 only and B * Hq <= 65535 (else ATTN_ERR_UNSUPPORTED); bad
+ * shapes, scale, pointers or alignment: ATTN_ERR_INVALID_ARG. Device pointers
+ * owned by the caller; asynchronous on `stream`.
+ */
+int attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+             const void *dout, float *delta, void *dq, void *dk, void *dv, int B, int Hq, int Hkv,
+             int S, int D, int causal, float scale, attn_stream_t stream);
+
 /* Size of the library's fixed scratch array used by attn_ring_fwd_static. */
 #define SEQATTN_RING_SCRATCH_BYTES (64ull << 20) /* 64 MiB */
 

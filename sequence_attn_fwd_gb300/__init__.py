@@ -22,7 +22,7 @@ import ctypes
 
 from ._lib import AttnBlock, AttnError, lib
 
-__all__ = ["attn_fwd", "attn_partial", "attn_partial_blocks", "attn_fwd_varlen", "attn_fwd_fp8", "lse_merge",
+__all__ = ["attn_fwd", "attn_partial", "attn_partial_blocks", "attn_fwd_varlen", "attn_fwd_fp8", "attn_bwd", "lse_merge",
            "ring_attn_fwd", "ring_attn_fwd_static", "EmulatedRing",
            "query_device_error", "AttnError", "lib", "RING_SCRATCH_BYTES"]
 
@@ -214,6 +214,32 @@ def attn_fwd_fp8(q8: torch.Tensor, k8: torch.Tensor, vt8: torch.Tensor, q_scale:
                           _stream_handle(q8.device))
     _check(st, "attn_fwd_fp8")
     return out, lse
+
+
+def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
+             dout: torch.Tensor, causal: bool = False, scale: float | None = None,
+             dq: torch.Tensor | None = None, dk: torch.Tensor | None = None, dv: torch.Tensor | None = None,
+             delta: torch.Tensor | None = None):
+    """Gradients (dQ, dK, dV) of attn_fwd(q, k, v) for the output gradient dout,
+    from the forward's o and lse (bf16 [B,Hq,S,128] q / o / dout, [B,Hkv,S,128]
+    k / v, fp32 lse [B,Hq,S]). delta is an optional fp32 [B,Hq,S] workspace."""
+    _require(q.dim() == 4 and k.dim() == 4 and v.shape == k.shape, "expected [B,H,S,D] tensors")
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    _require(o.shape == q.shape and dout.shape == q.shape and lse.shape == (B, Hq, S), "shape mismatch")
+    for t in (q, k, v, o, dout):
+        _require(t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous(), "bf16 contiguous CUDA tensors")
+    _require(lse.dtype == torch.float32 and lse.is_contiguous(), "lse must be contiguous fp32")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    delta = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device) if delta is None else delta
+    st = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                      delta.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, S, D,
+                      int(bool(causal)), scale, _stream_handle(q.device))
+    _check(st, "attn_bwd")
+    return dq, dk, dv
 
 
 def quantize_e4m3(x: torch.Tensor, scale: float) -> torch.Tensor:

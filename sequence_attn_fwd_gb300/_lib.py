@@ -14,7 +14,7 @@ LIB_PATH = os.path.join(_PKG, "lib", "libseqattn.so")
 # Every function the public header include/seqattn.h declares.
 EXPORTS = ["attn_fwd", "attn_partial", "lse_merge", "attn_query_device_error",
            "attn_status_string", "attn_last_cuda_error", "attn_ring_fwd_static",
-           "attn_debug_expire_wait", "attn_debug_exp2", "attn_partial_blocks", "attn_fwd_varlen", "attn_fwd_fp8"]
+           "attn_debug_expire_wait", "attn_debug_exp2", "attn_partial_blocks", "attn_fwd_varlen", "attn_fwd_fp8", "attn_bwd"]
 
 STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
           3: "ATTN_ERR_CUDA", 4: "ATTN_ERR_TIMEOUT"}
@@ -60,6 +60,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.attn_fwd_varlen.restype = ctypes.c_int
     L.attn_fwd_fp8.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, F, F, F, P]
     L.attn_fwd_fp8.restype = ctypes.c_int
+    L.attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P]
+    L.attn_bwd.restype = ctypes.c_int
     for name in ("attn_fwd", "attn_partial", "lse_merge", "attn_query_device_error",
                  "attn_last_cuda_error"):
         getattr(L, name).restype = ctypes.c_int

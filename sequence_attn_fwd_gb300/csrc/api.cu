@@ -239,6 +239,44 @@ int check_common(const void *q, const void *k, const void *v, const void *o, con
 
 extern "C" {
 
+int attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+             const void *dout, float *delta, void *dq, void *dk, void *dv, int B, int Hq, int Hkv,
+             int S, int D, int causal, float scale, attn_stream_t stream) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || S < 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (!scale_ok(scale)) return ATTN_ERR_INVALID_ARG;
+  if (D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (S > kMaxRowsPerHead) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Hq > 65535) return ATTN_ERR_UNSUPPORTED;  // grid rows
+  if (B == 0 || S == 0) return ATTN_OK;
+  const void *ptrs16[] = {q, k, v, o, dout, dq, dk, dv};
+  for (const void *ptr : ptrs16)
+    if (!ptr || !aligned16(ptr)) return ATTN_ERR_INVALID_ARG;
+  if (!lse || !delta || (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(delta) & 3u))
+    return ATTN_ERR_INVALID_ARG;
+  CUtensorMap tq, tk, tv, tdo;
+  const long long heads = static_cast<long long>(B) * Hq, kv_heads = static_cast<long long>(B) * Hkv;
+  const long long hs = static_cast<long long>(S) * D;
+  if (!make_map(&tq, q, D, S, heads, hs) || !make_map(&tk, k, D, S, kv_heads, hs) ||
+      !make_map(&tv, v, D, S, kv_heads, hs) || !make_map(&tdo, dout, D, S, heads, hs))
+    return cuda_fail(cudaErrorInvalidValue);
+  seqattn::BwdParams p{};
+  p.lse = lse;
+  p.delta = delta;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.S = S;
+  p.scale = scale;
+  p.causal = causal;
+  cudaError_t e = seqattn::launch_attention_bwd(tq, tk, tv, tdo, o, dout, delta, p,
+                                                reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
 int attn_fwd_fp8(const void *q8, const void *k8, const void *vt8, void *o, float *lse, int B, int Hq,
                  int Hkv, int S, int D, int causal, float scale, float q_scale, float k_scale,
                  float v_scale, attn_stream_t stream) {

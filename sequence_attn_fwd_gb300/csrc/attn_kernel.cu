@@ -434,6 +434,7 @@ cudaError_t launch_dispatch(int D, bool f32_out, const CUtensorMap &tq, const CU
 }  // namespace seqattn
 
 #include "attn_2sm.cuh"
+#include "attn_bwd.cuh"
 
 namespace seqattn {
 
@@ -469,6 +470,31 @@ cudaError_t launch_attention_blocks(int D, bool f32_out, const CUtensorMap &tq,
                                     const CUtensorMap &to, const AttnParams &p,
                                     const BlockTable &tbl, cudaStream_t stream) {
   return launch_dispatch(D, f32_out, tq, tk, tv, to, p, tbl, tbl.item_start[tbl.n], stream);
+}
+
+cudaError_t launch_attention_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                                 const CUtensorMap &tdo, const void *o, const void *dout,
+                                 float *delta, const BwdParams &p, cudaStream_t stream) {
+  const long long nrows = static_cast<long long>(p.B) * p.Hq * p.S;
+  if (nrows == 0) return cudaSuccess;
+  long long blocks = (nrows + 7) / 8;  // 8 warps of 256 threads, a row per warp
+  const long long cap = static_cast<long long>(sm_count()) * 8;
+  if (blocks > cap) blocks = cap;
+  bwd::delta_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16 *>(o), static_cast<const __nv_bfloat16 *>(dout), delta, nrows);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const unsigned n_tiles = static_cast<unsigned>((p.S + bwd::kRows - 1) / bwd::kRows);
+  for (int dq = 0; dq < 2; ++dq) {
+    auto kernel = dq ? bwd::attn_bwd_kernel<true> : bwd::attn_bwd_kernel<false>;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bwd::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(n_tiles, static_cast<unsigned>(p.B * (dq ? p.Hq : p.Hkv)));
+    kernel<<<grid, bwd::kThreads, bwd::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 // A one-CTA kernel waiting on an mbarrier that nothing ever arrives at, with

@@ -55,6 +55,23 @@ cudaError_t launch_attention(int D, bool f32_out, bool pair, const CUtensorMap &
                              const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                              const CUtensorMap &tm_o, const AttnParams &p, cudaStream_t stream);
 
+// Backward (head dim 128): gradients of a forward whose O and lse are given.
+struct BwdParams {
+  const float *lse;    // [B*Hq, S] natural log (the forward's)
+  const float *delta;  // [B*Hq, S] workspace: <dO_i, O_i>, written by the first kernel
+  void *dq, *dk, *dv;  // bf16 [B*Hq, S, D], [B*Hkv, S, D] x 2
+  int B, Hq, Hkv, S;
+  float scale;         // softmax scale
+  int causal;
+};
+
+// delta, then dK / dV (grid: key tiles x B*Hkv), then dQ (grid: query tiles x
+// B*Hq); maps over bf16 [heads][S][128], box 64 x 128 x 1, 128-byte swizzle.
+cudaError_t launch_attention_bwd(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                                 const CUtensorMap &tm_v, const CUtensorMap &tm_do,
+                                 const void *o, const void *dout, float *delta,
+                                 const BwdParams &p, cudaStream_t stream);
+
 // e4m3 attention (D = 128, bf16 O): tq / tk over e4m3 [heads][S][128] with
 // box 128 x 128 x 1, tvt over V^T e4m3 [kv heads][128][S] with box 128 (keys)
 // x 128 x 1, all 128-byte swizzle; p.scale_log2 includes the Q and K scales,

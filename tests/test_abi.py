@@ -33,7 +33,7 @@ def test_header_declares_the_boundary():
                                            "attn_status_string", "attn_last_cuda_error",
                                            "attn_ring_fwd_static", "attn_debug_expire_wait",
                                            "attn_debug_exp2", "attn_partial_blocks", "attn_fwd_varlen",
-                                           "attn_fwd_fp8"])
+                                           "attn_fwd_fp8", "attn_bwd"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -169,4 +169,16 @@ def test_attn_fwd_fp8_argument_checks(lib):
     assert run(S=100) == 2  # V^T rows must be 16-byte multiples
     assert run(qs=0.0) == 1 and run(vs=float("inf")) == 1
     assert run(Hq=3, Hkv=2) == 1 and run(causal=3) == 1
+    assert run(S=0) == 0
+
+
+def test_attn_bwd_argument_checks(lib):
+    def run(S=256, D=128, Hq=2, Hkv=1, B=1, q=FAKE, delta=FAKE, scale=0.1):
+        return lib.attn_bwd(q, FAKE, FAKE, FAKE, FAKE, FAKE, delta, FAKE, FAKE, FAKE, B, Hq, Hkv, S, D, 1,
+                            ctypes.c_float(scale), None)
+
+    assert run(D=64) == 2
+    assert run(B=2048, Hq=64, Hkv=64) == 2  # more than 65535 query heads
+    assert run(Hq=3, Hkv=2) == 1 and run(scale=-1.0) == 1
+    assert run(q=FAKE + 8) == 1 and run(delta=FAKE + 2) == 1 and run(q=0) == 1
     assert run(S=0) == 0

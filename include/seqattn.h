@@ -233,7 +233,7 @@ int attn_fwd_fp8(const void *q8, const void *k8, const void *vt8, void *o, float
  *   lse         fp32 [B, Hq, S] from attn_fwd (natural log)
  *   delta       fp32 [B, Hq, S] workspace (written, then read)
  *   dq          bf16 [B, Hq, S, 128];  dk, dv  bf16 [B, Hkv, S, 128]  (outputs)
- * Head dim 128 only and B * Hq <= 65535 (else ATTN_ERR_UNSUPPORTED); bad
+ * Head dim 128 only and S <= 65535 * 128 (else ATTN_ERR_UNSUPPORTED); bad
  * shapes, scale, pointers or alignment: ATTN_ERR_INVALID_ARG. Device pointers
  * owned by the caller; asynchronous on `stream`.
  */

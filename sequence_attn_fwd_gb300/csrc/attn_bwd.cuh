@@ -18,12 +18,15 @@
 //   dQ          one CTA per 128-row query tile: Q and dO stay, the visible key
 //               tiles stream through; S = Q K^T, dP = dO V^T, dS in TMEM, and
 //               dQ += dS K.
-// Both matrix kernels: warp 9 TMA producer, warp 8 MMA issuer (one thread),
-// warps 0-7 the element-wise pass. Every wait is bounded.
+// Both matrix kernels: warp 17 TMA producer, warp 16 MMA issuer (one thread),
+// warps 0-15 the element-wise pass (four warpgroups, two per 64-column half
+// of the tile, 32 columns each). Every wait is bounded.
 #pragma once
 #include <cuda_bf16.h>
 #include <math.h>
 #include <stdint.h>
+
+#include <type_traits>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -36,12 +39,12 @@ constexpr int kRows = 128;                      // tile rows (keys or queries)
 constexpr int kTileBytes = kRows * kD * 2;      // 32 KB: two 128-byte column blocks
 constexpr int kColBlock = kRows * 128;          // 16 KB
 constexpr int kStages = 4;                      // ring slots of 32 KB
-constexpr int kThreads = 320;
-constexpr int kMmaWarp = 8, kTmaWarp = 9;
+constexpr int kThreads = 576;
+constexpr int kMmaWarp = 16, kTmaWarp = 17;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// barriers: stay_full, full[S], empty[S], st_full, pt_full, acc_done
-constexpr int kNumBarriers = 1 + 2 * kStages + 3;
+// barriers: stay_full, full[S], empty[S], st_full[2], pt_full[2], acc_done
+constexpr int kNumBarriers = 1 + 2 * kStages + 5;
 constexpr int kSmemBytes = 1024 + 2 * kTileBytes + kStages * kTileBytes + 2 * 2 * kRows * 4 +
                            8 * kNumBarriers + 16;
 
@@ -52,9 +55,10 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap *map, 
   tma_load_3d(dst + kColBlock, map, bar, 64, row, head);
 }
 
-// S (or S^T) = A B^T over D = 128: A, B K-major tiles in shared memory.
+// One 64-column half of S (or S^T) = A B^T over D = 128: A a 128-row K-major
+// tile, B the 64 rows of a K-major tile starting at `b` (a multiple of 8 rows).
 __device__ __forceinline__ void mma_rows_dot(uint32_t d_tmem, uint32_t a, uint32_t b) {
-  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, false);
+  constexpr uint32_t idesc = idesc_bf16_f32(128, 64, false);
 #pragma unroll
   for (int kk = 0; kk < kD / 16; ++kk) {
     const uint32_t off = (kk / 4) * kColBlock + (kk % 4) * 32;
@@ -63,25 +67,30 @@ __device__ __forceinline__ void mma_rows_dot(uint32_t d_tmem, uint32_t a, uint32
   }
 }
 
-// acc (+)= A_tmem B: A = 128 x 128 bf16 in TMEM (contraction over its
-// columns), B = 128 x 128 tile in shared memory whose rows are the contraction
-// index (N-contiguous operand). A's 128 contraction elements are packed as
-// bf16 pairs in two runs of 32 TMEM columns, at a_tmem and a_tmem + 64 (each
-// element-wise warpgroup packs its 64 columns over the first half of its own).
-__device__ __forceinline__ void mma_acc_tmem(uint32_t acc, uint32_t a_tmem, uint32_t b, bool first) {
+// acc (+)= A_h B_h for contraction half h: A = 128 x 128 bf16 in TMEM
+// (contraction over its columns), B = 128 x 128 tile in shared memory whose
+// rows are the contraction index (N-contiguous operand); half h covers
+// contraction elements [64h, 64h + 64). A's elements are packed as bf16 pairs:
+// the element-wise warpgroup of columns [32c, 32c + 32) packs them over the
+// first 16 of its own TMEM columns, so elements 16k..16k+15 sit in the 8
+// columns at a_tmem + 32(k/2) + 8(k%2).
+__device__ __forceinline__ void mma_acc_tmem(uint32_t acc, uint32_t a_tmem, uint32_t b, int h, bool first) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, kD, true);
 #pragma unroll
-  for (int kk = 0; kk < kRows / 16; ++kk)
-    mma_ts(acc, a_tmem + (kk / 4) * 64 + (kk % 4) * 8, sw128_desc(b + kk * 2048, kColBlock, 1024),
-           idesc, (first && kk == 0) ? 0u : 1u);
+  for (int k4 = 0; k4 < 4; ++k4) {
+    const int kk = 4 * h + k4;
+    mma_ts(acc, a_tmem + 64 * h + 32 * (k4 >> 1) + 8 * (k4 & 1), sw128_desc(b + kk * 2048, kColBlock, 1024), idesc,
+           (first && k4 == 0) ? 0u : 1u);
+  }
 }
 
-// One thread's row of a 128 x 128 fp32 TMEM accumulator, times `mul`, as bf16
-// into global memory (one 256-byte row). Every lane of the warp takes part in
-// the TMEM loads (they are warp-wide); only lanes with `valid` store.
+// NC columns of one thread's row of an fp32 TMEM accumulator, times `mul`,
+// as bf16 into global memory. Every lane of the warp takes part in the TMEM
+// loads (they are warp-wide); only lanes with `valid` store.
+template <int NC>
 __device__ __forceinline__ void store_acc_row(uint32_t taddr, float mul, __nv_bfloat16 *dst, bool valid) {
 #pragma unroll 1
-  for (int cb = 0; cb < kD / 32; ++cb) {
+  for (int cb = 0; cb < NC / 32; ++cb) {
     uint32_t r[32];
     tmem_ld32(taddr + 32 * cb, r);
     tmem_ld_wait(r);
@@ -150,14 +159,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar0 = smem_addr(bars);
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
   const int kBarStay = 0, kBarFull = 1, kBarEmpty = 1 + kStages, kBarSt = 1 + 2 * kStages,
-            kBarPt = kBarSt + 1, kBarAcc = kBarPt + 1;
+            kBarPt = kBarSt + 2, kBarAcc = kBarPt + 2;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int *err = &g_device_error;
   const int S = p.S, group = p.Hq / p.Hkv;
   const int n_tiles = (S + kRows - 1) / kRows;
-  const int tile = blockIdx.x;  // key tile (dK/dV) or query tile (dQ)
-  const int head = blockIdx.y;  // b*Hkv + hkv (dK/dV) or b*Hq + hq (dQ)
+  // heads vary fastest and the CTAs with the most iterations come first: low
+  // key tiles (dK/dV), high query tiles (causal dQ)
+  const int head = blockIdx.x;  // b*Hkv + hkv (dK/dV) or b*Hq + hq (dQ)
+  const int tile = (kDq && p.causal) ? n_tiles - 1 - static_cast<int>(blockIdx.y)
+                                     : static_cast<int>(blockIdx.y);  // key or query tile
   const int b = kDq ? head / p.Hq : head / p.Hkv;
   // dK/dV: iterations over (query head of the group, query tile >= this key
   // tile when causal); dQ: over key tiles <= this query tile when causal
@@ -180,8 +192,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarFull + s), 1);
       mbar_init(bar(kBarEmpty + s), 1);
     }
-    mbar_init(bar(kBarSt), 1);
-    mbar_init(bar(kBarPt), 8);  // one arrival per element-wise warp
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(bar(kBarSt + h), 1);
+      mbar_init(bar(kBarPt + h), 8);  // one arrival per warp of the two warpgroups of half h
+    }
     mbar_init(bar(kBarAcc), 1);
     *abort_flag = *reinterpret_cast<volatile int *>(err) != kErrNone;
     fence_barrier_init();
@@ -240,33 +254,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && !skip && n_iter > 0) {
       const uint32_t stay0 = smem_addr(sStay), stay1 = stay0 + kTileBytes;
       const uint32_t ring = smem_addr(sRing);
-      bool ok = mbar_wait(bar(kBarStay), 0, abort_flag, err);
-      for (int it = 0; ok && it < n_iter; ++it) {
+      // Half h of iteration it: S / dP columns [64h, 64h + 64) (element-wise
+      // warpgroup h), then the accumulations over that half. Each half's
+      // accumulation is issued once its warpgroup is done, followed by the
+      // next iteration's scores of the same half, so one warpgroup's
+      // element-wise pass overlaps the other half's MMAs.
+      auto wait_full = [&](int it) {
         const int c0 = 2 * it, c1 = 2 * it + 1;
-        const int s0 = c0 % kStages, s1 = c1 % kStages;
-        if (!mbar_wait(bar(kBarFull + s0), (c0 / kStages) & 1, abort_flag, err) ||
-            !mbar_wait(bar(kBarFull + s1), (c1 / kStages) & 1, abort_flag, err))
-          break;
+        const bool got = mbar_wait(bar(kBarFull + c0 % kStages), (c0 / kStages) & 1, abort_flag, err) &&
+                         mbar_wait(bar(kBarFull + c1 % kStages), (c1 / kStages) & 1, abort_flag, err);
         tc_fence_after();
-        const uint32_t r0 = ring + s0 * kTileBytes, r1 = ring + s1 * kTileBytes;
+        return got;
+      };
+      auto ring0 = [&](int it) { return ring + ((2 * it) % kStages) * kTileBytes; };
+      auto ring1 = [&](int it) { return ring + ((2 * it + 1) % kStages) * kTileBytes; };
+      auto scores = [&](int it, int h) {  // S = Q K_j^T, dP = dO V_j^T (or S^T = K Q_i^T, dP^T = V dO_i^T)
+        mma_rows_dot(tS + 64 * h, stay0, ring0(it) + 8192 * h);
+        mma_rows_dot(tDP + 64 * h, stay1, ring1(it) + 8192 * h);
+        mma_commit(bar(kBarSt + h));
+      };
+      auto accumulate = [&](int it, int h) {
         if (kDq) {
-          mma_rows_dot(tS, stay0, r0);   // S = Q K_j^T
-          mma_rows_dot(tDP, stay1, r1);  // dP = dO V_j^T
+          mma_acc_tmem(tAcc0, tS, ring0(it), h, it == 0 && h == 0);   // dQ += dS K_j
         } else {
-          mma_rows_dot(tS, stay0, r0);   // S^T = K Q_i^T
-          mma_rows_dot(tDP, stay1, r1);  // dP^T = V dO_i^T
+          mma_acc_tmem(tAcc0, tS, ring1(it), h, it == 0 && h == 0);   // dV += P^T dO_i
+          mma_acc_tmem(tAcc1, tDP, ring0(it), h, it == 0 && h == 0);  // dK += dS^T Q_i
         }
-        mma_commit(bar(kBarSt));
+      };
+      bool ok = mbar_wait(bar(kBarStay), 0, abort_flag, err) && wait_full(0);
+      if (ok) {
+        scores(0, 0);
+        scores(0, 1);
+      }
+      for (int it = 0; ok && it < n_iter; ++it) {
+        const bool more = it + 1 < n_iter;
         if (!mbar_wait(bar(kBarPt), it & 1, abort_flag, err)) break;
         tc_fence_after();
-        if (kDq) {
-          mma_acc_tmem(tAcc0, tS, r0, it == 0);   // dQ += dS K_j
-        } else {
-          mma_acc_tmem(tAcc0, tS, r1, it == 0);   // dV += P^T dO_i
-          mma_acc_tmem(tAcc1, tDP, r0, it == 0);  // dK += dS^T Q_i
+        accumulate(it, 0);
+        if (more) {
+          if (!wait_full(it + 1)) break;
+          scores(it + 1, 0);
         }
-        mma_commit(bar(kBarEmpty + s0));
-        mma_commit(bar(kBarEmpty + s1));
+        if (!mbar_wait(bar(kBarPt + 1), it & 1, abort_flag, err)) break;
+        tc_fence_after();
+        accumulate(it, 1);
+        mma_commit(bar(kBarEmpty + (2 * it) % kStages));
+        mma_commit(bar(kBarEmpty + (2 * it + 1) % kStages));
+        if (more) scores(it + 1, 1);
       }
       mma_commit(bar(kBarAcc));
       mbar_drain(bar(kBarAcc), 0, err);
@@ -274,10 +308,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ element-wise pass
-    const int g = warp >> 2;                       // column half of this warpgroup
+    const int wg = warp >> 2;                        // element-wise warpgroup 0-3
+    const int h = wg & 1;                            // 64-column half it serves
+    const int c_base = 64 * h + 32 * (wg >> 1);      // its 32 columns of the tile
     const int row_in_tile = (warp & 3) * 32 + lane;  // TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const int my_row = tile * kRows + row_in_tile;  // key (dK/dV) or query (dQ) of this thread
+    const int my_row = tile * kRows + row_in_tile;   // key (dK/dV) or query (dQ) of this thread
     const float c2 = p.scale * kLog2e;
     // dQ: this query row's lse (log2 units) and delta, once
     float row_lse2 = INFINITY, row_delta = 0.f;
@@ -285,74 +321,99 @@ __global__ void __launch_bounds__(kThreads, 1)
       row_lse2 = p.lse[static_cast<size_t>(head) * S + my_row] * kLog2e;
       row_delta = p.delta[static_cast<size_t>(head) * S + my_row];
     }
+    // dK/dV: thread t < 32 of the warpgroup carries the lse (log2 units) and
+    // delta of query column c_base + t of the streamed tile, loaded one
+    // iteration ahead so that the load latency hides behind an iteration
+    const int vec_col = c_base + (threadIdx.x & 127);
+    const bool vec_thread = !kDq && (threadIdx.x & 127) < 32;
+    float nxt_lse2 = INFINITY, nxt_delta = 0.f;
+    auto load_vec = [&](int it) {
+      int r, qh;
+      stream_of(it, r, qh);
+      const int i = r + vec_col;
+      nxt_lse2 = (i < S) ? p.lse[static_cast<size_t>(qh) * S + i] * kLog2e : INFINITY;
+      nxt_delta = (i < S) ? p.delta[static_cast<size_t>(qh) * S + i] : 0.f;
+    };
+    if (vec_thread && n_iter > 0) load_vec(0);
     bool ok = !skip;
     for (int it = 0; it < n_iter; ++it) {
       int srow, q_head;
       stream_of(it, srow, q_head);
       float *vec = sVec + (it & 1) * 2 * kRows;  // [lse2 | delta] of the streamed query tile
-      if (!kDq) {
-        const int t = threadIdx.x & 127;
-        if (t < 64) {
-          const int col = 64 * g + t, i = srow + col;
-          vec[col] = (i < S) ? p.lse[static_cast<size_t>(q_head) * S + i] * kLog2e : INFINITY;
-          vec[kRows + col] = (i < S) ? p.delta[static_cast<size_t>(q_head) * S + i] : 0.f;
-        }
+      if (vec_thread) {
+        vec[vec_col] = nxt_lse2;
+        vec[kRows + vec_col] = nxt_delta;
+        if (it + 1 < n_iter) load_vec(it + 1);
       }
-      bool got = ok && mbar_wait(bar(kBarSt), it & 1, abort_flag, err);
-      got = named_bar_and(1 + g, 128, __all_sync(0xffffffffu, got));  // also publishes vec
+      // the mask matters only on tiles that cross the end of the sequence or
+      // the causal diagonal
+      const int base = tile * kRows;
+      const bool need_mask = base + kRows > S || srow + kRows > S ||
+                             (p.causal && (kDq ? srow + kRows > base : srow < base + kRows));
+      bool got = ok && mbar_wait(bar(kBarSt + h), it & 1, abort_flag, err);
+      got = named_bar_and(1 + wg, 128, __all_sync(0xffffffffu, got));  // also publishes vec
       if (!got) break;
       tc_fence_after();
-      uint32_t pk_a[32], pk_b[32];  // bf16 pairs: P^T and dS^T (dK/dV) or dS (dQ)
+      // 16 columns at col0: P and dS as bf16 pairs, written over the first 16
+      // of this warpgroup's columns (chunk c to c_base + 8c), which it has
+      // already read
+      auto chunk = [&](auto mask_tag, int c) {
+        constexpr bool kMask = decltype(mask_tag)::value;
+        const int col0 = c_base + 16 * c;
+        uint32_t sr[16], dr[16];
+        tmem_ld16(tS + lane_off + col0, sr);
+        tmem_ld16(tDP + lane_off + col0, dr);
+        float lv[16], dl[16];
+        if (!kDq) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int col0 = 64 * g + 32 * h;
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tS + lane_off + col0, sr);
-        tmem_ld32(tDP + lane_off + col0, dr);
+          for (int i = 0; i < 4; ++i) {
+            const float4 a4 = reinterpret_cast<const float4 *>(vec + col0)[i];
+            const float4 d4 = reinterpret_cast<const float4 *>(vec + kRows + col0)[i];
+            lv[4 * i] = a4.x, lv[4 * i + 1] = a4.y, lv[4 * i + 2] = a4.z, lv[4 * i + 3] = a4.w;
+            dl[4 * i] = d4.x, dl[4 * i + 1] = d4.y, dl[4 * i + 2] = d4.z, dl[4 * i + 3] = d4.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) lv[i] = row_lse2, dl[i] = row_delta;
+        }
         tmem_ld_wait(sr);
         tmem_ld_wait(dr);
+        uint32_t pa[8], pb[8];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
+        for (int e = 0; e < 16; e += 2) {
           float pv[2], dsv[2];
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const int col = col0 + e + u;
-            const int other = srow + col;  // the query (dK/dV) or key (dQ) of this column
-            int q_i, k_j;
-            float lse2, dl;
-            if (kDq) {
-              q_i = my_row;
-              k_j = other;
-              lse2 = row_lse2;
-              dl = row_delta;
-            } else {
-              q_i = other;
-              k_j = my_row;
-              lse2 = vec[col];
-              dl = vec[kRows + col];
+            float pr = ex2_approx(__uint_as_float(sr[e + u]) * c2 - lv[e + u]);
+            if (kMask) {
+              const int other = srow + col0 + e + u;  // the query (dK/dV) or key (dQ) of this column
+              const int q_i = kDq ? my_row : other, k_j = kDq ? other : my_row;
+              if (!(q_i < S && k_j < S && (!p.causal || k_j <= q_i))) pr = 0.f;
             }
-            const bool vis = q_i < S && k_j < S && (!p.causal || k_j <= q_i);
-            const float pr = vis ? ex2_approx(__uint_as_float(sr[e + u]) * c2 - lse2) : 0.f;
             pv[u] = pr;
-            dsv[u] = pr * (__uint_as_float(dr[e + u]) - dl);
+            dsv[u] = pr * (__uint_as_float(dr[e + u]) - dl[e + u]);
           }
-          pk_a[16 * h + e / 2] = pack_bf16x2(pv[0], pv[1]);
-          pk_b[16 * h + e / 2] = pack_bf16x2(dsv[0], dsv[1]);
+          pa[e / 2] = pack_bf16x2(pv[0], pv[1]);
+          pb[e / 2] = pack_bf16x2(dsv[0], dsv[1]);
         }
-      }
-      // the warpgroup's 64 columns become 32 TMEM columns of bf16 pairs, written
-      // over the first half of its own columns (the other warpgroup may still
-      // be reading its own)
-      if (kDq) {
-        tmem_st32(tS + lane_off + 64 * g, pk_b);  // dS over S
+        if (kDq) {
+          tmem_st8(tS + lane_off + c_base + 8 * c, pb);  // dS over S
+        } else {
+          tmem_st8(tS + lane_off + c_base + 8 * c, pa);   // P^T over S^T
+          tmem_st8(tDP + lane_off + c_base + 8 * c, pb);  // dS^T over dP^T
+        }
+      };
+      if (need_mask) {
+        chunk(std::true_type{}, 0);
+        chunk(std::true_type{}, 1);
       } else {
-        tmem_st32(tS + lane_off + 64 * g, pk_a);  // P^T over S^T
-        tmem_st32(tDP + lane_off + 64 * g, pk_b); // dS^T over dP^T
+        chunk(std::false_type{}, 0);
+        chunk(std::false_type{}, 1);
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarPt));
+      if (lane == 0) mbar_arrive(bar(kBarPt + h));
     }
     // ------------------------------------------------------------ epilogue
     bool done = ok && n_iter > 0 && mbar_wait(bar(kBarAcc), 0, abort_flag, err);
@@ -361,16 +422,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warp-uniform branches only around the TMEM loads; the row bound guards the stores
     const bool valid = my_row < S;
     const size_t row_off = static_cast<size_t>(head) * S + (valid ? my_row : 0);
-    if (kDq) {
-      if (g == 0) {  // dQ = scale dS K
-        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.dq) + row_off * kD;
-        if (done) store_acc_row(tAcc0 + lane_off, p.scale, dst, valid);
-        else if (valid) for (int d = 0; d < kD; ++d) dst[d] = __float2bfloat16(0.f);
-      }
-    } else {
-      __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(g == 0 ? p.dv : p.dk) + row_off * kD;
-      if (done) store_acc_row((g == 0 ? tAcc0 : tAcc1) + lane_off, g == 0 ? 1.f : p.scale, dst, valid);
-      else if (valid) for (int d = 0; d < kD; ++d) dst[d] = __float2bfloat16(0.f);
+    if (kDq) {  // dQ = scale dS K: warpgroup w stores columns [32w, 32w + 32)
+      __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.dq) + row_off * kD + 32 * wg;
+      if (done) store_acc_row<32>(tAcc0 + lane_off + 32 * wg, p.scale, dst, valid);
+      else if (valid) for (int d = 0; d < 32; ++d) dst[d] = __float2bfloat16(0.f);
+    } else {  // warpgroups 0, 1: dV columns [0, 64), [64, 128); 2, 3: dK (times scale)
+      const bool is_dk = wg >= 2;
+      const int cofs = 64 * (wg & 1);
+      __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(is_dk ? p.dk : p.dv) + row_off * kD + cofs;
+      if (done) store_acc_row<64>((is_dk ? tAcc1 : tAcc0) + lane_off + cofs, is_dk ? p.scale : 1.f, dst, valid);
+      else if (valid) for (int d = 0; d < 64; ++d) dst[d] = __float2bfloat16(0.f);
     }
   }
 

@@ -489,7 +489,7 @@ cudaError_t launch_attention_bwd(const CUtensorMap &tq, const CUtensorMap &tk, c
     auto kernel = dq ? bwd::attn_bwd_kernel<true> : bwd::attn_bwd_kernel<false>;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bwd::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const dim3 grid(n_tiles, static_cast<unsigned>(p.B * (dq ? p.Hq : p.Hkv)));
+    const dim3 grid(static_cast<unsigned>(p.B * (dq ? p.Hq : p.Hkv)), n_tiles);
     kernel<<<grid, bwd::kThreads, bwd::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

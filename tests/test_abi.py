@@ -178,7 +178,7 @@ def test_attn_bwd_argument_checks(lib):
                             ctypes.c_float(scale), None)
 
     assert run(D=64) == 2
-    assert run(B=2048, Hq=64, Hkv=64) == 2  # more than 65535 query heads
+    assert run(S=65536 * 128) == 2  # more than 65535 tiles of 128 rows
     assert run(Hq=3, Hkv=2) == 1 and run(scale=-1.0) == 1
     assert run(q=FAKE + 8) == 1 and run(delta=FAKE + 2) == 1 and run(q=0) == 1
     assert run(S=0) == 0

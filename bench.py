@@ -43,6 +43,7 @@ sys.path.insert(0, ROOT)
 import workloads  # noqa: E402
 
 METRIC = "attention fwd TFLOP/s (causal-adjusted) & % BF16 peak; lse_merge GB/s & % HBM"
+METRIC_BWD = "attention bwd TFLOP/s (causal-adjusted, 2.5x the forward's FLOPs) & % BF16 peak"
 DEFAULT_WORKLOAD = "ring8_b2h32s4096d128_causal"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129e6
@@ -94,6 +95,7 @@ def merge_algorithmic_bytes(w: workloads.Workload, out_bytes: int = 2) -> int:
 
 
 KERNEL_SOURCES = {
+    "attn_bwd": ["attn_kernel.cu", "attn_bwd.cuh", "ptx.cuh"],
     "attn_partial": ["attn_kernel.cu", "attn_common.cuh", "ptx.cuh"],
     "attn_partial_blocks": ["attn_kernel.cu", "attn_common.cuh", "ptx.cuh"],
     "attn_fwd_varlen": ["attn_kernel.cu", "attn_common.cuh", "ptx.cuh"],
@@ -376,6 +378,124 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int):
     }
 
 
+def run_ours_backward(args, w: workloads.Workload, rank: int, world: int):
+    """The backward step: one attn_bwd call (delta pre-pass, dK/dV kernel, dQ
+    kernel) from the forward's O and lse, for a seeded dO. FLOPs counted as
+    2.5x the forward's (the five products of the backward: S, dP, dV, dK, dQ;
+    the kernels recompute S and dP once more for dQ, which is not counted)."""
+    import sequence_attn_fwd_gb300 as sa
+
+    if w.P > 1 or w.varlen or w.D != 128 or args.dtype != "bf16":
+        raise SystemExit("--backward runs single-pass head-dim-128 bf16 workloads")
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    q_h, k_h, v_h = workloads.make_qkv(w)
+    do_h = workloads.make_dout(w)
+    q, k, v, do = q_h.to(dev), k_h.to(dev), v_h.to(dev), do_h.to(dev)
+    o, lse = sa.attn_fwd(q, k, v, causal=w.causal)  # untimed: the backward's inputs
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    delta = torch.empty_like(lse)
+
+    def step(qq, kk, vv, oo, ll, dd):
+        sa.attn_bwd(qq, kk, vv, oo, ll, dd, causal=w.causal, dq=dq, dk=dk, dv=dv, delta=delta)
+
+    F = 2.5 * w.attention_flops()
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    t_end = time.time() + args.warmup_seconds
+    n = 0
+    while n < args.warmup or time.time() < t_end:
+        step(q, k, v, o, lse, do)
+        n += 1
+        if n % 8 == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        step(q, k, v, o, lse, do)
+        evs[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    sa.query_device_error(dev)
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1))
+    call_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    value = world * F * args.steps / (elapsed_ms * 1e-3) / 1e12
+
+    e2e = None
+    if rank == 0 and not args.no_e2e:  # pinned host Q, K, V, O, lse, dO in; dQ, dK, dV out
+        ins_h = [t.pin_memory() for t in (q_h, k_h, v_h, o.cpu(), lse.cpu(), do_h)]
+        ins_d = [torch.empty_like(t, device=dev) for t in ins_h]
+        outs_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
+
+        def e2e_step():
+            for d_, h_ in zip(ins_d, ins_h):
+                d_.copy_(h_, non_blocking=True)
+            step(*ins_d)
+            for h_, d_ in zip(outs_h, (dq, dk, dv)):
+                h_.copy_(d_, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        n_e2e = max(3, min(args.steps, 20))
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b_.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = a.elapsed_time(b_) / n_e2e
+        e2e = {"value": F / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in ins_h),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in outs_h)}
+        del ins_d
+
+    peaks, peak_src = load_peaks()
+    achieved = F / (call_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "traffic": measured_traffic("attn_bwd", w.name),
+                "kernel": "attn_bwd (one call: delta_kernel, attn_bwd_kernel<dK/dV>, attn_bwd_kernel<dQ>)",
+                "peak_source": f"{peak_src} bf16 burst", "launch_ms": call_ms}
+    return {"value": value, "ms_per_step": elapsed_ms / args.steps, "e2e": e2e, "roofline": roofline,
+            "merge": None, "gpu_launches": 3 * args.steps, "clocks": clocks}
+
+
+def oracle_backward_sample(w: workloads.Workload, budget_s: float, prefix: int = 1024):
+    """Times the fp64 oracle's backward on the first `prefix` positions of one
+    (batch, query head) and its KV head per call, heads in turn, until about
+    budget_s seconds of CPU work are done; FLOPs 2.5x the forward's on the
+    prefix. Returns (TFLOP/s, seconds, calls, threads)."""
+    import oracle
+
+    q, k, v = workloads.make_qkv(w, S=prefix)
+    do = workloads.make_dout(w, S=prefix)
+    threads = oracle.default_threads()
+    g = w.Hq // w.Hkv
+    pairs = prefix * (prefix + 1) / 2 if w.causal else prefix * prefix
+    flops, calls = 0.0, 0
+    t0 = time.perf_counter()
+    while True:
+        b, h = divmod(calls % (w.B * w.Hq), w.Hq)
+        oracle.attention_backward(q[b:b + 1, h:h + 1], k[b:b + 1, h // g:h // g + 1],
+                                  v[b:b + 1, h // g:h // g + 1], do[b:b + 1, h:h + 1], w.causal,
+                                  threads=threads)
+        flops += 2.5 * 4.0 * w.D * pairs
+        calls += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    secs = time.perf_counter() - t0
+    return flops / secs / 1e12, secs, calls, threads
+
+
 # ----------------------------------------------------------------- the CPU oracle arm
 
 def oracle_sample(w: workloads.Workload, budget_s: float, q=None, k=None, v=None, max_calls: int | None = None):
@@ -513,6 +633,9 @@ def main(argv=None):
     ap.add_argument("--partials", default="grouped", choices=["grouped", "per-chunk"],
                     help="ring workloads: the P chunks' partials in one attn_partial_blocks launch "
                          "(default) or one attn_partial launch per chunk")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward (attn_bwd: dQ, dK, dV) instead of the forward step "
+                         "(single-pass workloads)")
     ap.add_argument("--ring-schedule", action="store_true",
                     help="instead of the step: per-hop device times of the emulated causal ring, "
                          "contiguous vs zigzag layout (ring workloads)")
@@ -545,16 +668,22 @@ def main(argv=None):
             return 1
         print(json.dumps(run_ring_schedules(args, w)), flush=True)
         return 0
-    r = run_ours(args, w, rank, world)
+    r = run_ours_backward(args, w, rank, world) if args.backward else run_ours(args, w, rank, world)
     if rank == 0:
         cpu = None
-        if world == 1 and not args.no_cpu_baseline:
+        if world == 1 and not args.no_cpu_baseline and args.backward:
+            val, secs, calls, threads = oracle_backward_sample(w, args.cpu_baseline_budget)
+            cpu = {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                   "sample": f"the oracle's backward on the first 1024 positions of {calls} "
+                             f"(batch, query head) pairs in turn ({secs:.1f} s), fp64 chain rule"}
+        elif world == 1 and not args.no_cpu_baseline:
             val, secs, heads, threads = oracle_sample(w, args.cpu_baseline_budget)
             unit = "(sequence, head), sequences and heads" if w.varlen else "(batch, head), heads"
             cpu = {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                    "sample": f"{heads} seeded query rows of the workload (up to 256 per {unit} "
                              f"in turn; {secs:.1f} s), fp64 definition"}
-        line = {"metric": METRIC, "value": r["value"], "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        metric = METRIC_BWD if args.backward else METRIC
+        line = {"metric": metric, "value": r["value"], "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
                 "config": workload_config(w, args.partials), "roofline": r["roofline"], "merge": r["merge"],

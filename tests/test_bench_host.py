@@ -7,6 +7,7 @@ import os
 
 import numpy as np
 import pytest
+import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
 
@@ -120,3 +121,21 @@ def test_ring_time_from_hops():
     assert r["ring_ms"] == 5.0 and r["device_ms_total"] == 8.0
     assert r["hop_spread_max_over_mean"] == [1.5, 1.0]
     assert r["balance"] == 0.8
+
+
+def test_dout_is_seeded_and_independent_of_qkv():
+    w = workloads.WORKLOADS["gqa_b1hq28hkv4s32768d128_causal"]
+    d1 = workloads.make_dout(w, S=64)
+    d2 = workloads.make_dout(w, S=64)
+    q, _, _ = workloads.make_qkv(w, S=64)
+    assert d1.shape == (w.B, w.Hq, 64, w.D) and d1.dtype == torch.bfloat16
+    assert torch.equal(d1, d2) and not torch.equal(d1, q)
+    assert abs(float(d1.float().std()) - 1.0) < 0.05
+
+
+def test_backward_sample_counts_two_and_a_half_forward_flops():
+    """The oracle backward sample's FLOPs: 2.5 x 4 D per visible pair of the prefix."""
+    w = workloads.WORKLOADS["gqa_b1hq28hkv4s32768d128_causal"]
+    rate, secs, calls, _ = bench.oracle_backward_sample(w, 0.0, prefix=32)
+    assert calls == 1
+    assert rate * 1e12 * secs == pytest.approx(2.5 * 4 * w.D * 32 * 33 / 2, rel=1e-9)

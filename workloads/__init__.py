@@ -18,8 +18,10 @@ Recipe (every draw is reproducible from the integer seed):
   * "extra" spawns the stream for the key-boost positions (a distinct
     sample of floor(frac * S) sequence positions whose keys are multiplied
     by 2, exact in bf16, for every batch and KV head), the stream for the
-    sampled query rows, the stream for synthetic merge partials, and the
-    stream for the sequence lengths of a packed (varlen) workload.
+    sampled query rows, the stream for synthetic merge partials, the stream
+    for the sequence lengths of a packed (varlen) workload, and the stream
+    of the output gradient dO for the backward (drawn like Q: one
+    child stream per (batch, query head), N(0, 1) rounded to bf16).
   * A packed workload (B = 1, S = total tokens) draws sequence lengths
     round(exp(N(ln 1536, 0.8^2))) clipped to [128, 8192] until the total is
     reached, the last one cut to fit: a training-style length mix with many
@@ -72,7 +74,7 @@ class Workload:
         return f * 0.5 if self.causal else f
 
 
-# The five workloads the attention path is checked and measured on.
+# The six workloads the attention path is checked and measured on.
 WORKLOADS = {
     w.name: w
     for w in [
@@ -123,6 +125,12 @@ def make_qkv(w: Workload, S: int | None = None):
         pos = boost_positions(w, S)
         k[:, :, pos, :] = k[:, :, pos, :] * 2  # exact: a bf16 exponent bump
     return q, k, v
+
+
+def make_dout(w: Workload, S: int | None = None) -> torch.Tensor:
+    """Seeded bf16 output gradient dO [B,Hq,S,D] on the CPU (backward inputs)."""
+    S = w.S if S is None else S
+    return _normal_heads(_streams(w.seed)[3].spawn(5)[4], w.B, w.Hq, S, w.D)
 
 
 def boost_positions(w: Workload, S: int | None = None) -> np.ndarray:

@@ -12,7 +12,7 @@ import torch
 
 import oracle
 import workloads
-from tests.parity import LSE_TOL, O_TOL, check_lse, check_o, gather_rows
+from tests.parity import LSE_TOL, O_TOL, bwd_bound, bwd_ratio, check_lse, check_o, gather_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -356,40 +356,6 @@ def test_attn_fwd_fp8_against_oracle(sa, shape):
     assert float(err.mean()) <= 0.25 * float(bound.mean())
 
 
-def bwd_bound(q, k, v, dout, o_used, causal, scale):
-    """Per-element bounds on the backward's error (numpy fp64, small shapes).
-    The kernel's approximations beyond fp32 accumulation: P and dS rounded to
-    bf16 before their products (2^-9 relative each), delta computed from the O
-    it is given (the bf16 forward output, whose exact difference from the exact
-    O is known here), and the bf16 rounding of the results. With dd_i = |<dO_i,
-    O_used_i - O_i>| (plus its bf16 share): |d dS_ij| <= 2^-9 |dS_ij| + P_ij dd_i,
-    and each gradient's error is the sum of its terms' errors, + 2^-8 |result|."""
-    qn, kn, vn, dn, on = (t.double().numpy() for t in (q, k, v, dout, o_used))
-    B, Hq, S, D = qn.shape
-    g = Hq // kn.shape[1]
-    bq = np.zeros_like(qn)
-    bk = np.zeros_like(kn)
-    bv = np.zeros_like(vn)
-    mask = np.tril(np.ones((S, S), dtype=bool)) if causal else np.ones((S, S), dtype=bool)
-    for b in range(B):
-        for h in range(Hq):
-            hk = h // g
-            s = np.where(mask, scale * qn[b, h] @ kn[b, hk].T, -np.inf)
-            p = np.exp(s - s.max(axis=1, keepdims=True))
-            p /= p.sum(axis=1, keepdims=True)
-            o_ex = p @ vn[b, hk]
-            dp = dn[b, h] @ vn[b, hk].T
-            delta = (dn[b, h] * o_ex).sum(axis=1, keepdims=True)
-            ds = p * (dp - delta)
-            dd = np.abs((dn[b, h] * (on[b, h] - o_ex)).sum(axis=1, keepdims=True))
-            dd += 2.0 ** -8 * (np.abs(dn[b, h]) * np.abs(on[b, h])).sum(axis=1, keepdims=True)
-            e_ds = 2.0 ** -9 * np.abs(ds) + p * dd
-            bv[b, hk] += 2.0 ** -9 * p.T @ np.abs(dn[b, h])
-            bk[b, hk] += scale * e_ds.T @ np.abs(qn[b, h])
-            bq[b, h] = scale * e_ds @ np.abs(kn[b, hk])
-    return bq, bk, bv
-
-
 @pytest.mark.parametrize("shape", [(1, 2, 2, 256, True), (1, 4, 2, 300, True), (2, 2, 1, 200, False)],
                          ids=["s256c", "gqa_s300c", "b2_s200"])
 def test_attn_bwd_against_oracle(sa, shape):
@@ -406,10 +372,7 @@ def test_attn_bwd_against_oracle(sa, shape):
     rq, rk, rv = oracle.attention_backward(q, k, v, dout, causal)
     bq, bk, bv = bwd_bound(q, k, v, dout, o.cpu(), causal, 1.0 / math.sqrt(D))
     for name, got, ref, bnd in (("dq", dq, rq, bq), ("dk", dk, rk, bk), ("dv", dv, rv, bv)):
-        g = got.double().cpu().numpy()
-        assert np.isfinite(g).all(), name
-        tol = bnd + 2.0 ** -8 * np.abs(ref) + 1e-4
-        worst = float((np.abs(g - ref) / tol).max())
+        worst = bwd_ratio(got, ref, bnd)
         assert worst <= 1.0, f"{name}: error exceeds its bound by {worst:.2f}x"
 
 

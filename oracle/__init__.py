@@ -14,6 +14,8 @@ lse_merge(o_parts, lse_parts)
 attention_backward(q, k, v, dout, causal, scale=None, threads=None)
     fp64 gradients (dQ, dK, dV) of attention for the output gradient dO
     (bf16 [B,Hq,S,D]); see attn_oracle.c.
+attention_backward_dq_rows(q, k, v, dout, causal, rows, scale=None, threads=None)
+    fp64 dQ of selected query rows ([B*Hq, n] indices) only, row by row.
 """
 from __future__ import annotations
 
@@ -56,6 +58,9 @@ def _load():
         lib.oracle_attention_backward.argtypes = [P, P, P, P] + [ctypes.c_int] * 6 + [
             ctypes.c_double, P, P, P, ctypes.c_int]
         lib.oracle_attention_backward.restype = ctypes.c_int
+        lib.oracle_attention_backward_dq_rows.argtypes = [P, P, P, P] + [ctypes.c_int] * 6 + [
+            ctypes.c_double, P, ctypes.c_int, P, ctypes.c_int]
+        lib.oracle_attention_backward_dq_rows.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -134,3 +139,25 @@ def attention_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dout: 
     if rc != 0:
         raise ValueError("oracle_attention_backward rejected its arguments")
     return dq, dk, dv
+
+
+def attention_backward_dq_rows(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dout: torch.Tensor,
+                               causal: bool, rows: np.ndarray, scale: float | None = None,
+                               threads: int | None = None) -> np.ndarray:
+    """fp64 dQ [B*Hq, n, D] of the query rows rows[b*Hq + h] (int64 [B*Hq, n])
+    of each (batch, query head): the chain rule of attention_backward for one
+    row at a time (attn_oracle.c)."""
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    assert k.shape == (B, Hkv, S, D) and v.shape == k.shape and dout.shape == q.shape and Hq % Hkv == 0
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    assert rows.ndim == 2 and rows.shape[0] == B * Hq
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    qb, kb, vb, db = _bits(q), _bits(k), _bits(v), _bits(dout)
+    out = np.empty((B * Hq, rows.shape[1], D), dtype=np.float64)
+    rc = _load().oracle_attention_backward_dq_rows(qb.ctypes.data, kb.ctypes.data, vb.ctypes.data, db.ctypes.data,
+                                                   B, Hq, Hkv, S, D, int(bool(causal)), scale, rows.ctypes.data,
+                                                   rows.shape[1], out.ctypes.data, int(threads or default_threads()))
+    if rc != 0:
+        raise ValueError("oracle_attention_backward_dq_rows rejected its arguments")
+    return out

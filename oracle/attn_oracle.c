@@ -351,3 +351,100 @@ int oracle_attention_backward(const uint16_t *q, const uint16_t *k, const uint16
     }
     return rc;
 }
+
+/*
+ * dQ of selected query rows only: the same chain rule for one row at a time
+ * (dQ_i needs only row i's softmax and dP), for checking outputs of problems
+ * too large to differentiate whole. rows: int64 [B*Hq][n] row indices (each
+ * in [0, S)); dq_rows: doubles [B*Hq][n][D] (output). Returns 0, or -1 on
+ * invalid arguments.
+ */
+typedef struct {
+    const uint16_t *q, *k, *v, *dout;
+    int B, Hq, Hkv, S, D, causal;
+    double scale;
+    const long long *rows;
+    int n;
+    double *dq_rows;
+    int nthreads, tid;
+} dq_rows_job;
+
+static void *dq_rows_worker(void *arg)
+{
+    const dq_rows_job *j = (const dq_rows_job *)arg;
+    const int S = j->S, D = j->D, group = j->Hq / j->Hkv;
+    double *p = (double *)malloc(sizeof(double) * (size_t)(S > 0 ? S : 1));
+    double *dp = (double *)malloc(sizeof(double) * (size_t)(S > 0 ? S : 1));
+    if (!p || !dp) {
+        free(p);
+        free(dp);
+        return (void *)1;
+    }
+    for (long long item = j->tid; item < (long long)j->B * j->Hq * j->n; item += j->nthreads) {
+        const long long bh = item / j->n;
+        const int b = (int)(bh / j->Hq), hq = (int)(bh % j->Hq), hkv = hq / group;
+        const long long i = j->rows[item];
+        const uint16_t *kh = j->k + ((long long)b * j->Hkv + hkv) * S * D;
+        const uint16_t *vh = j->v + ((long long)b * j->Hkv + hkv) * S * D;
+        const uint16_t *qi = j->q + (bh * S + i) * D, *doi = j->dout + (bh * S + i) * D;
+        double *dqi = j->dq_rows + item * D;
+        const long long nvis = j->causal ? i + 1 : S;
+        for (int d = 0; d < D; d++) dqi[d] = 0.0;
+        double m = -INFINITY;
+        for (long long t = 0; t < nvis; t++) {
+            double dot = 0.0;
+            for (int d = 0; d < D; d++) dot += bf16_to_double(qi[d]) * bf16_to_double(kh[t * D + d]);
+            p[t] = j->scale * dot;
+            if (p[t] > m) m = p[t];
+        }
+        double l = 0.0;
+        for (long long t = 0; t < nvis; t++) {
+            p[t] = exp(p[t] - m);
+            l += p[t];
+        }
+        for (long long t = 0; t < nvis; t++) p[t] /= l;
+        double psum = 0.0;
+        for (long long t = 0; t < nvis; t++) {
+            double dot = 0.0;
+            for (int d = 0; d < D; d++) dot += bf16_to_double(doi[d]) * bf16_to_double(vh[t * D + d]);
+            dp[t] = dot;
+            psum += p[t] * dot;
+        }
+        for (long long t = 0; t < nvis; t++) {
+            const double ds = p[t] * (dp[t] - psum);
+            for (int d = 0; d < D; d++) dqi[d] += j->scale * ds * bf16_to_double(kh[t * D + d]);
+        }
+    }
+    free(p);
+    free(dp);
+    return NULL;
+}
+
+int oracle_attention_backward_dq_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                      const uint16_t *dout, int B, int Hq, int Hkv, int S, int D,
+                                      int causal, double scale, const long long *rows, int n,
+                                      double *dq_rows, int nthreads)
+{
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || S < 0 || D <= 0 || n < 0) return -1;
+    for (long long t = 0; t < (long long)B * Hq * n; t++)
+        if (rows[t] < 0 || rows[t] >= S) return -1;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    pthread_t th[256];
+    dq_rows_job jobs[256];
+    int rc = 0;
+    for (int t = 0; t < nthreads; t++) {
+        jobs[t] = (dq_rows_job){q, k, v, dout, B, Hq, Hkv, S, D, causal, scale, rows, n, dq_rows, nthreads, t};
+        if (pthread_create(&th[t], NULL, dq_rows_worker, &jobs[t]) != 0) {
+            nthreads = t;
+            rc = -1;
+            break;
+        }
+    }
+    for (int t = 0; t < nthreads; t++) {
+        void *ret = NULL;
+        pthread_join(th[t], &ret);
+        if (ret) rc = -1;
+    }
+    return rc;
+}

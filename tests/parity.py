@@ -56,15 +56,27 @@ def gather_rows(t: torch.Tensor, rows: np.ndarray) -> torch.Tensor:
     return torch.gather(t, 2, idx).cpu()
 
 
-def bwd_bound(q, k, v, dout, o_used, causal, scale):
+def _np(t) -> np.ndarray:
+    return t.detach().double().cpu().numpy() if isinstance(t, torch.Tensor) else np.asarray(t, dtype=np.float64)
+
+
+# Relative error of the P the backward kernels form: bf16 rounding (2^-9)
+# plus a 2^-12 budget for the fp32 score, exp2 and lse rounding ahead of it.
+P_REL = 2.0 ** -9 + 2.0 ** -12
+
+
+def bwd_bound(q, k, v, dout, causal, scale, o_in):
     """Per-element bounds on the backward's error (numpy fp64, small shapes).
-    The kernel's approximations beyond fp32 accumulation: P and dS rounded to
-    bf16 before their products (2^-9 relative each), delta computed from the O
-    it is given (the bf16 forward output, whose exact difference from the exact
-    O is known here), and the bf16 rounding of the results. With dd_i = |<dO_i,
-    O_used_i - O_i>| (plus its bf16 share): |d dS_ij| <= 2^-9 |dS_ij| + P_ij dd_i,
-    and each gradient's error is the sum of its terms' errors, + 2^-8 |result|."""
-    qn, kn, vn, dn, on = (t.double().numpy() for t in (q, k, v, dout, o_used))
+    The kernel's approximations: P formed in fp32 from the fp32 scores and
+    the given lse, then rounded to bf16 (P_REL relative); dP = dO V^T in fp32
+    (error <= 2^-16 sum_d |dO_id v_jd|); delta formed in fp32 from the O it is
+    given (o_in), off from the exact delta_i by at most
+    dd_i = |<dO_i, o_in_i - O_i>| + 2^-16 sum_d |dO_id o_in_id|; dS rounded to
+    bf16 (2^-9); the bf16 rounding of the results (added by bwd_ratio). So
+    |d dS_ij| <= (P_REL + 2^-9) |dS_ij| + P_ij (dd_i + 2^-16 sum_d |dO_id v_jd|),
+    |d P_ij| <= P_REL P_ij, and each gradient's error is the sum of its terms'
+    errors."""
+    qn, kn, vn, dn, on = (_np(t) for t in (q, k, v, dout, o_in))
     B, Hq, S, D = qn.shape
     g = Hq // kn.shape[1]
     bq = np.zeros_like(qn)
@@ -81,13 +93,41 @@ def bwd_bound(q, k, v, dout, o_used, causal, scale):
             dp = dn[b, h] @ vn[b, hk].T
             delta = (dn[b, h] * o_ex).sum(axis=1, keepdims=True)
             ds = p * (dp - delta)
-            dd = np.abs((dn[b, h] * (on[b, h] - o_ex)).sum(axis=1, keepdims=True))
-            dd += 2.0 ** -8 * (np.abs(dn[b, h]) * np.abs(on[b, h])).sum(axis=1, keepdims=True)
-            e_ds = 2.0 ** -9 * np.abs(ds) + p * dd
-            bv[b, hk] += 2.0 ** -9 * p.T @ np.abs(dn[b, h])
+            dd = (np.abs((dn[b, h] * (on[b, h] - o_ex)).sum(axis=1, keepdims=True))
+                  + 2.0 ** -16 * np.abs(dn[b, h] * on[b, h]).sum(axis=1, keepdims=True))
+            e_dp = 2.0 ** -16 * np.abs(dn[b, h]) @ np.abs(vn[b, hk]).T
+            e_ds = (P_REL + 2.0 ** -9) * np.abs(ds) + p * (dd + e_dp)
+            bv[b, hk] += P_REL * p.T @ np.abs(dn[b, h])
             bk[b, hk] += scale * e_ds.T @ np.abs(qn[b, h])
             bq[b, h] = scale * e_ds @ np.abs(kn[b, hk])
     return bq, bk, bv
+
+
+def bwd_dq_rows_bound(q, k, v, dout, causal, scale, rows: np.ndarray, o_rows_in) -> np.ndarray:
+    """bwd_bound's dQ bound for the query rows rows[b*Hq + h] only ([B*Hq, n, D]),
+    row by row, for problems too large to bound whole; o_rows_in [B*Hq, n, D]
+    holds the O rows the kernel was given."""
+    B, Hq, S, D = q.shape
+    g = Hq // k.shape[1]
+    o_in = _np(o_rows_in)
+    out = np.empty((B * Hq, rows.shape[1], D))
+    for bh in range(B * Hq):
+        b, h = divmod(bh, Hq)
+        kn = k[b, h // g].double().numpy()
+        vn = v[b, h // g].double().numpy()
+        for r, i in enumerate(rows[bh]):
+            n = int(i) + 1 if causal else S
+            qi = q[b, h, i].double().numpy()
+            di = dout[b, h, i].double().numpy()
+            s = scale * (kn[:n] @ qi)
+            p = np.exp(s - s.max())
+            p /= p.sum()
+            o_ex = p @ vn[:n]
+            ds = p * (vn[:n] @ di - di @ o_ex)
+            dd = abs(float(di @ (o_in[bh, r] - o_ex))) + 2.0 ** -16 * float(np.abs(di * o_in[bh, r]).sum())
+            e_dp = 2.0 ** -16 * (np.abs(vn[:n]) @ np.abs(di))
+            out[bh, r] = scale * ((P_REL + 2.0 ** -9) * np.abs(ds) + p * (dd + e_dp)) @ np.abs(kn[:n])
+    return out
 
 
 def bwd_ratio(got: torch.Tensor, ref: np.ndarray, bound: np.ndarray) -> float:

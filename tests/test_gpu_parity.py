@@ -12,7 +12,7 @@ import torch
 
 import oracle
 import workloads
-from tests.parity import LSE_TOL, O_TOL, bwd_bound, bwd_ratio, check_lse, check_o, gather_rows
+from tests.parity import LSE_TOL, O_TOL, bwd_bound, bwd_dq_rows_bound, bwd_ratio, check_lse, check_o, gather_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -359,21 +359,63 @@ def test_attn_fwd_fp8_against_oracle(sa, shape):
 @pytest.mark.parametrize("shape", [(1, 2, 2, 256, True), (1, 4, 2, 300, True), (2, 2, 1, 200, False)],
                          ids=["s256c", "gqa_s300c", "b2_s200"])
 def test_attn_bwd_against_oracle(sa, shape):
-    """dQ, dK, dV from the GPU forward's O and lse against the oracle's exact
-    gradients, each element within the bound derived in bwd_bound."""
+    """dQ, dK, dV (from the oracle's O and lse as the backward's inputs) against
+    the oracle's exact gradients, each element within the bound derived in
+    bwd_bound."""
     B, Hq, Hkv, S, causal = shape
     D = 128
     q, k, v = workloads.make_qkv(adhoc(B, Hq, Hkv, S, D, causal, seed=71))
     dout, _, _ = workloads.make_qkv(adhoc(B, Hq, Hq, S, D, causal, seed=72))
     qd, kd, vd, dod = to_dev(q, k, v, dout)
-    o, lse = sa.attn_fwd(qd, kd, vd, causal=causal)
+    # the forward's O and lse as the backward's inputs, from the oracle (O rounded to bf16)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=causal)
+    o_in = torch.from_numpy(o_ref).to(torch.bfloat16)
+    o, lse = to_dev(o_in, torch.from_numpy(lse_ref).float())
     dq, dk, dv = sa.attn_bwd(qd, kd, vd, o, lse, dod, causal=causal)
     torch.cuda.synchronize()
     rq, rk, rv = oracle.attention_backward(q, k, v, dout, causal)
-    bq, bk, bv = bwd_bound(q, k, v, dout, o.cpu(), causal, 1.0 / math.sqrt(D))
+    bq, bk, bv = bwd_bound(q, k, v, dout, causal, 1.0 / math.sqrt(D), o_in)
     for name, got, ref, bnd in (("dq", dq, rq, bq), ("dk", dk, rk, bk), ("dv", dv, rv, bv)):
         worst = bwd_ratio(got, ref, bnd)
         assert worst <= 1.0, f"{name}: error exceeds its bound by {worst:.2f}x"
+
+
+def test_attn_bwd_full_size_gqa(sa):
+    """The backward at the full size of the GQA workload, in the configuration
+    bench.py --backward times (the GPU forward's O and lse as its inputs): on 8
+    seeded query rows per head, the forward's O rows within the forward
+    tolerance of the oracle's and dQ against the oracle's row-by-row dQ within
+    the derived bound (delta's offset taken from those checked O rows); dV
+    against the exact identity sum_j dV_j = sum over the group's query heads of
+    sum_i dO_i (the rows of P sum to 1), within 2^-8 of the summed magnitudes;
+    every gradient finite."""
+    w = workloads.WORKLOADS["gqa_b1hq28hkv4s32768d128_causal"]
+    q, k, v = workloads.make_qkv(w)
+    dout = workloads.make_dout(w)
+    qd, kd, vd, dod = to_dev(q, k, v, dout)
+    o, lse = sa.attn_fwd(qd, kd, vd, causal=w.causal)
+    dq, dk, dv = sa.attn_bwd(qd, kd, vd, o, lse, dod, causal=w.causal)
+    torch.cuda.synchronize()
+    sa.query_device_error()
+    for t in (dq, dk, dv):
+        assert bool(torch.isfinite(t).all())
+    rows = workloads.sample_query_rows(w, n=8)
+    pick = lambda t: torch.stack([t[b, h, torch.from_numpy(rows[b * w.Hq + h]).to(t.device)]
+                                  for b in range(w.B) for h in range(w.Hq)])
+    o_rows = pick(o).cpu()
+    o_ref, _ = oracle.attention(q, k, v, w.causal, rows=rows)
+    check_o(o_rows.reshape(o_ref.shape), o_ref)
+    ref = oracle.attention_backward_dq_rows(q, k, v, dout, w.causal, rows)
+    bnd = bwd_dq_rows_bound(q, k, v, dout, w.causal, w.scale, rows, o_rows)
+    got = pick(dq)
+    worst = bwd_ratio(got, ref, bnd)
+    assert worst <= 1.0, f"dQ rows: error exceeds the bound by {worst:.2f}x"
+    g = w.Hq // w.Hkv
+    dv_sum = dv.double().sum(dim=2).cpu().numpy()                                       # [B, Hkv, D]
+    do_sum = dout.double().reshape(w.B, w.Hkv, g * w.S, w.D).sum(dim=2).numpy()
+    tol = 2.0 ** -8 * (dout.double().abs().reshape(w.B, w.Hkv, g * w.S, w.D).sum(dim=2).numpy()
+                       + dv.double().abs().sum(dim=2).cpu().numpy())
+    assert (np.abs(dv_sum - do_sum) <= tol).all(), float((np.abs(dv_sum - do_sum) / tol).max())
 
 
 # ----------------------------------------------------------------- full-size workloads

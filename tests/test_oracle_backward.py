@@ -75,3 +75,18 @@ def test_gqa_is_the_group_sum_of_the_expanded_problem():
     np.testing.assert_allclose(dq, dq2, rtol=0, atol=1e-13)
     np.testing.assert_allclose(dk, dk2.reshape(1, Hkv, Hq // Hkv, 24, 8).sum(axis=2), rtol=0, atol=1e-13)
     np.testing.assert_allclose(dv, dv2.reshape(1, Hkv, Hq // Hkv, 24, 8).sum(axis=2), rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_dq_rows_equal_the_whole_backward(causal):
+    """The row-by-row dQ (used on problems too large to differentiate whole)
+    gives the whole backward's dQ rows, in the same order of operations."""
+    Hq, Hkv, S, D = 4, 2, 50, 16
+    q, k, v, d = qkvd(Hq, Hkv, S, D, 5)
+    dq, _, _ = oracle.attention_backward(q, k, v, d, causal)
+    rows = np.stack([np.array([0, 7, 31, 49]) for _ in range(Hq)])
+    got = oracle.attention_backward_dq_rows(q, k, v, d, causal, rows)
+    for h in range(Hq):
+        np.testing.assert_array_equal(got[h], dq[0, h, rows[h]])
+    with pytest.raises(ValueError):
+        oracle.attention_backward_dq_rows(q, k, v, d, causal, rows + 1)  # row 50 is out of range

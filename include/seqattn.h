@@ -33,6 +33,8 @@
 #ifndef SEQATTN_H
 #define SEQATTN_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -240,6 +242,45 @@ int attn_fwd_fp8(const void *q8, const void *k8, const void *vt8, void *o, float
 int attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
              const void *dout, float *delta, void *dq, void *dk, void *dv, int B, int Hq, int Hkv,
              int S, int D, int causal, float scale, attn_stream_t stream);
+
+/*
+ * attn_ring_fwd_host_workspace_bytes -- bytes of device workspace that
+ * attn_ring_fwd_host needs for these sizes (device copies of Q, K, V, the
+ * fp32 partials when P > 1, and O and lse), or 0 for invalid sizes.
+ */
+size_t attn_ring_fwd_host_workspace_bytes(int B, int Hq, int Hkv, int S, int D, int P);
+
+/*
+ * attn_ring_fwd_host -- the ring-emulated forward from host buffers to host
+ * buffers: the Ring-Attention pass of the page "Ulysses与Ring-Attention序列
+ * 并行技术详解" with each hop's K/V chunk arriving over the host link. Q and
+ * then every K/V chunk are copied to the device on an internal copy stream;
+ * chunk j's attn_partial starts on `stream` as soon as chunk j has arrived, so
+ * the copies of later chunks overlap it; then lse_merge and the copies of O
+ * and lse back to the host, on `stream`. P = 1: one attn_fwd after the copies.
+ *   q, k, v   host bf16 [B, Hq, S, D], [B, Hkv, S, D], [B, Hkv, S, D]
+ *             (page-locked, or the copies cannot overlap anything)
+ *   o, lse    host bf16 [B, Hq, S, D], fp32 [B, Hq, S] (outputs, page-locked
+ *             likewise)
+ *   workspace device memory, 256-byte aligned, at least
+ *             attn_ring_fwd_host_workspace_bytes(B, Hq, Hkv, S, D, P) bytes,
+ *             owned by the caller; no other call may use it at the same time.
+ * Asynchronous: the call returns once everything is queued; o and lse hold
+ * the result when `stream` reaches the end of the call. The uploads of a call
+ * wait for the work queued on `stream` before it (and so for an earlier call
+ * on that stream that used the same workspace); a caller that alternates two
+ * (stream, workspace, o/lse) sets overlaps one call's uploads with the
+ * previous call's compute and downloads. Host-side inputs must stay unchanged,
+ * and outputs unread, until then.
+ * Rules as attn_fwd (D 64 or 128), plus 1 <= P <= 64 and S % P == 0. Errors as
+ * attn_fwd; ATTN_ERR_INVALID_ARG also for a null pointer or a workspace that is
+ * too small or misaligned. Chunk j's partial is attn_partial with
+ * ATTN_PARTIAL_SKIP_EMPTY, so results equal those of the device-side ring with
+ * one attn_partial per chunk.
+ */
+int attn_ring_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse, void *workspace,
+                       size_t workspace_bytes, int B, int Hq, int Hkv, int S, int D, int P, int causal,
+                       float scale, attn_stream_t stream);
 
 /* Size of the library's fixed scratch array used by attn_ring_fwd_static. */
 #define SEQATTN_RING_SCRATCH_BYTES (64ull << 20) /* 64 MiB */

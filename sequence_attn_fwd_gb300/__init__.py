@@ -23,7 +23,8 @@ import ctypes
 from ._lib import AttnBlock, AttnError, lib
 
 __all__ = ["attn_fwd", "attn_partial", "attn_partial_blocks", "attn_fwd_varlen", "attn_fwd_fp8", "attn_bwd", "lse_merge",
-           "ring_attn_fwd", "ring_attn_fwd_static", "EmulatedRing",
+           "ring_attn_fwd", "ring_attn_fwd_static", "ring_attn_fwd_host", "ring_host_workspace_bytes",
+           "EmulatedRing",
            "query_device_error", "AttnError", "lib", "RING_SCRATCH_BYTES"]
 
 RING_SCRATCH_BYTES = 64 << 20  # the library's fixed scratch array for ring_attn_fwd_static
@@ -442,6 +443,60 @@ def ring_attn_fwd_static(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: i
     st = lib.attn_ring_fwd_static(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                                   B, Hq, Hkv, S, D, int(P), int(bool(causal)), scale, _stream_handle(q.device))
     _check(st, "attn_ring_fwd_static")
+    return out, lse
+
+
+def ring_host_workspace_bytes(B: int, Hq: int, Hkv: int, S: int, D: int, P: int) -> int:
+    """Device workspace bytes ring_attn_fwd_host needs (attn_ring_fwd_host_workspace_bytes)."""
+    n = lib.attn_ring_fwd_host_workspace_bytes(B, Hq, Hkv, S, D, P)
+    _require(n > 0, "invalid sizes")
+    return int(n)
+
+
+def ring_attn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, causal: bool = False,
+                       scale: float | None = None, out: torch.Tensor | None = None,
+                       lse: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                       device: torch.device | None = None, synchronize: bool = True):
+    """The ring-emulated forward from host tensors to host tensors
+    (attn_ring_fwd_host): Q and each K/V chunk are uploaded on the library's
+    copy stream, each chunk's partial starts on the current stream as soon as
+    its chunk arrives, then the merge and the downloads of O and lse.
+    q, k, v: CPU bf16 [B, H, S, D] (pinned for the copies to overlap);
+    out, lse: CPU outputs (pinned ones are allocated when not given);
+    workspace: a uint8 CUDA tensor of at least ring_host_workspace_bytes(...)
+    bytes (allocated when not given). With synchronize=False the call returns
+    once the work is queued on the current stream; the outputs are complete
+    when that stream reaches it."""
+    _require(q.dim() == 4 and k.dim() == 4 and v.shape == k.shape, "expected [B,H,S,D] tensors")
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    for t in (q, k, v):
+        _require(t.dtype == torch.bfloat16 and t.device.type == "cpu" and t.is_contiguous(),
+                 "q, k, v must be contiguous bf16 CPU tensors")
+    device = device or torch.device("cuda", torch.cuda.current_device())
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    if lse is None:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32).pin_memory()
+    _require(out.device.type == "cpu" and out.dtype == torch.bfloat16 and out.shape == q.shape
+             and out.is_contiguous(), "out must be a contiguous bf16 CPU tensor shaped like q")
+    _require(lse.device.type == "cpu" and lse.dtype == torch.float32 and lse.shape == (B, Hq, S)
+             and lse.is_contiguous(), "lse must be a contiguous fp32 CPU tensor [B, Hq, S]")
+    need = ring_host_workspace_bytes(B, Hq, Hkv, S, D, P)
+    if workspace is None:
+        # the library's copy stream writes the workspace, which torch's allocator
+        # does not track: a workspace allocated here must outlive the work
+        _require(synchronize, "pass a workspace when synchronize=False")
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    _require(workspace.is_cuda and workspace.numel() * workspace.element_size() >= need,
+             "workspace must be a CUDA tensor of at least ring_host_workspace_bytes(...) bytes")
+    st = lib.attn_ring_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                B, Hq, Hkv, S, D, int(P), int(bool(causal)), scale, _stream_handle(device))
+    _check(st, "attn_ring_fwd_host")
+    if synchronize:
+        torch.cuda.current_stream(device).synchronize()
     return out, lse
 
 

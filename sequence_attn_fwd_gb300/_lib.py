@@ -14,7 +14,8 @@ LIB_PATH = os.path.join(_PKG, "lib", "libseqattn.so")
 # Every function the public header include/seqattn.h declares.
 EXPORTS = ["attn_fwd", "attn_partial", "lse_merge", "attn_query_device_error",
            "attn_status_string", "attn_last_cuda_error", "attn_ring_fwd_static",
-           "attn_debug_expire_wait", "attn_debug_exp2", "attn_partial_blocks", "attn_fwd_varlen", "attn_fwd_fp8", "attn_bwd"]
+           "attn_debug_expire_wait", "attn_debug_exp2", "attn_partial_blocks", "attn_fwd_varlen", "attn_fwd_fp8", "attn_bwd",
+           "attn_ring_fwd_host_workspace_bytes", "attn_ring_fwd_host"]
 
 STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
           3: "ATTN_ERR_CUDA", 4: "ATTN_ERR_TIMEOUT"}
@@ -50,6 +51,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.attn_last_cuda_error.argtypes = []
     L.attn_ring_fwd_static.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, P]
     L.attn_ring_fwd_static.restype = ctypes.c_int
+    L.attn_ring_fwd_host_workspace_bytes.argtypes = [I, I, I, I, I, I]
+    L.attn_ring_fwd_host_workspace_bytes.restype = ctypes.c_size_t
+    L.attn_ring_fwd_host.argtypes = [P, P, P, P, P, P, ctypes.c_size_t, I, I, I, I, I, I, I, F, P]
+    L.attn_ring_fwd_host.restype = ctypes.c_int
     L.attn_debug_expire_wait.argtypes = [ctypes.c_uint, P]
     L.attn_debug_expire_wait.restype = ctypes.c_int
     L.attn_debug_exp2.argtypes = [P, P, ctypes.c_longlong, ctypes.c_int, P]

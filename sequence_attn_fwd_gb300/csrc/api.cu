@@ -512,3 +512,123 @@ extern "C" int attn_ring_fwd_static(const void *q, const void *k, const void *v,
   }
   return lse_merge(o_parts, lse_parts, P, o, ATTN_BF16, lse, B, Hq, S, D, stream);
 }
+
+namespace {
+
+// Byte offsets inside the workspace of attn_ring_fwd_host, each part 256-byte aligned.
+struct HostLayout {
+  size_t q, k, v, o_parts, lse_parts, o, lse, total;
+};
+
+bool host_layout(int B, int Hq, int Hkv, int S, int D, int P, HostLayout *L) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || S < 0 || (D != 64 && D != 128) || P < 1 || P > 64) return false;
+  const size_t rows = static_cast<size_t>(B) * Hq * S, kv_rows = static_cast<size_t>(B) * Hkv * S;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up_256(off + bytes);
+    return at;
+  };
+  L->q = take(rows * D * 2);
+  L->k = take(kv_rows * D * 2);
+  L->v = take(kv_rows * D * 2);
+  L->o_parts = take(P > 1 ? static_cast<size_t>(P) * rows * D * sizeof(float) : 0);
+  L->lse_parts = take(P > 1 ? static_cast<size_t>(P) * rows * sizeof(float) : 0);
+  L->o = take(rows * D * 2);
+  L->lse = take(rows * sizeof(float));
+  L->total = off;
+  return true;
+}
+
+// One non-blocking copy stream per device, created on the first call there.
+std::mutex g_copy_stream_mutex;
+cudaStream_t g_copy_stream[kMaxDevices] = {};
+
+int copy_stream(cudaStream_t *out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_copy_stream_mutex);
+  if (!g_copy_stream[dev]) {
+    cudaStream_t s = nullptr;
+    e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_copy_stream[dev] = s;
+  }
+  *out = g_copy_stream[dev];
+  return ATTN_OK;
+}
+
+// `waiter` waits for the work queued on `signaller` so far.
+cudaError_t stream_wait(cudaStream_t waiter, cudaStream_t signaller) {
+  cudaEvent_t ev = nullptr;
+  cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+  if (e != cudaSuccess) return e;
+  e = cudaEventRecord(ev, signaller);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(waiter, ev, 0);
+  const cudaError_t d = cudaEventDestroy(ev);  // released once the event completes
+  return e != cudaSuccess ? e : d;
+}
+
+}  // namespace
+
+extern "C" size_t attn_ring_fwd_host_workspace_bytes(int B, int Hq, int Hkv, int S, int D, int P) {
+  HostLayout L;
+  return host_layout(B, Hq, Hkv, S, D, P, &L) ? L.total : 0;
+}
+
+extern "C" int attn_ring_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse,
+                                  void *workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int S,
+                                  int D, int P, int causal, float scale, attn_stream_t stream) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || S < 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (!scale_ok(scale)) return ATTN_ERR_INVALID_ARG;
+  if (P < 1 || P > 64 || S % P != 0) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (S > kMaxRowsPerHead) return ATTN_ERR_UNSUPPORTED;
+  HostLayout L;
+  if (!host_layout(B, Hq, Hkv, S, D, P, &L)) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || S == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !lse || !workspace) return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < L.total) return ATTN_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream), cs = nullptr;
+  int rc = copy_stream(&cs);
+  if (rc != ATTN_OK) return rc;
+  unsigned char *ws = static_cast<unsigned char *>(workspace);
+  unsigned char *qd = ws + L.q, *kd = ws + L.k, *vd = ws + L.v;
+  float *o_parts = reinterpret_cast<float *>(ws + L.o_parts), *lse_parts = reinterpret_cast<float *>(ws + L.lse_parts);
+  void *od = ws + L.o;
+  float *lsed = reinterpret_cast<float *>(ws + L.lse);
+  const size_t rows = static_cast<size_t>(B) * Hq * S;
+  const size_t head_bytes = static_cast<size_t>(S) * D * 2;  // one head's K or V rows
+  const int C = S / P;
+  const size_t chunk_bytes = static_cast<size_t>(C) * D * 2;
+  // the uploads start after the work queued on `stream` before this call
+  cudaError_t e = stream_wait(cs, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(qd, q, rows * D * 2, cudaMemcpyHostToDevice, cs);
+  if (e != cudaSuccess) return cuda_fail(e);
+  for (int j = 0; j < P; ++j) {
+    // chunk j of every (batch, KV head): B*Hkv rows of chunk_bytes, head_bytes apart
+    const size_t off = static_cast<size_t>(j) * chunk_bytes;
+    e = cudaMemcpy2DAsync(kd + off, head_bytes, static_cast<const unsigned char *>(k) + off, head_bytes,
+                          chunk_bytes, static_cast<size_t>(B) * Hkv, cudaMemcpyHostToDevice, cs);
+    if (e == cudaSuccess)
+      e = cudaMemcpy2DAsync(vd + off, head_bytes, static_cast<const unsigned char *>(v) + off, head_bytes,
+                            chunk_bytes, static_cast<size_t>(B) * Hkv, cudaMemcpyHostToDevice, cs);
+    if (e == cudaSuccess) e = stream_wait(st, cs);  // chunk j (and Q) on the device
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (P > 1) {
+      rc = attn_partial(qd, kd + off, vd + off, 0, static_cast<long long>(j) * C, static_cast<long long>(S) * D,
+                        o_parts + static_cast<size_t>(j) * rows * D, lse_parts + static_cast<size_t>(j) * rows,
+                        B, Hq, Hkv, S, C, D, causal, scale, ATTN_PARTIAL_SKIP_EMPTY, stream);
+      if (rc != ATTN_OK) return rc;
+    }
+  }
+  rc = P > 1 ? lse_merge(o_parts, lse_parts, P, od, ATTN_BF16, lsed, B, Hq, S, D, stream)
+             : attn_fwd(qd, kd, vd, od, lsed, B, Hq, Hkv, S, D, causal, scale, stream);
+  if (rc != ATTN_OK) return rc;
+  e = cudaMemcpyAsync(o, od, rows * D * 2, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(lse, lsed, rows * sizeof(float), cudaMemcpyDeviceToHost, st);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}

@@ -33,7 +33,8 @@ def test_header_declares_the_boundary():
                                            "attn_status_string", "attn_last_cuda_error",
                                            "attn_ring_fwd_static", "attn_debug_expire_wait",
                                            "attn_debug_exp2", "attn_partial_blocks", "attn_fwd_varlen",
-                                           "attn_fwd_fp8", "attn_bwd"])
+                                           "attn_fwd_fp8", "attn_bwd",
+                                           "attn_ring_fwd_host_workspace_bytes", "attn_ring_fwd_host"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -181,4 +182,31 @@ def test_attn_bwd_argument_checks(lib):
     assert run(S=65536 * 128) == 2  # more than 65535 tiles of 128 rows
     assert run(Hq=3, Hkv=2) == 1 and run(scale=-1.0) == 1
     assert run(q=FAKE + 8) == 1 and run(delta=FAKE + 2) == 1 and run(q=0) == 1
+    assert run(S=0) == 0
+
+
+def test_ring_host_workspace_layout(lib):
+    """Device copies of Q, K, V, the fp32 partials (P > 1 only), O and lse, each
+    rounded up to 256 bytes."""
+    up = lambda n: (n + 255) // 256 * 256
+    B, Hq, Hkv, S, D, P = 2, 8, 2, 1000, 128, 8
+    rows, kv = B * Hq * S, B * Hkv * S
+    want = up(rows * D * 2) + 2 * up(kv * D * 2) + up(P * rows * D * 4) + up(P * rows * 4) + up(rows * D * 2) + up(rows * 4)
+    assert lib.attn_ring_fwd_host_workspace_bytes(B, Hq, Hkv, S, D, P) == want
+    assert lib.attn_ring_fwd_host_workspace_bytes(B, Hq, Hkv, S, D, 1) == (
+        up(rows * D * 2) + 2 * up(kv * D * 2) + up(rows * D * 2) + up(rows * 4))
+    for bad in ((B, Hq, Hkv, S, 96, P), (B, Hq, Hkv, S, D, 0), (B, Hq, Hkv, S, D, 65), (B, 0, Hkv, S, D, P)):
+        assert lib.attn_ring_fwd_host_workspace_bytes(*bad) == 0
+
+
+def test_ring_host_argument_checks(lib):
+    def run(S=512, P=4, D=128, ws=FAKE, ws_bytes=1 << 40, q=FAKE, scale=0.1, Hq=4, Hkv=2):
+        return lib.attn_ring_fwd_host(q, FAKE, FAKE, FAKE, FAKE, ws, ws_bytes, 1, Hq, Hkv, S, D, P, 1,
+                                      ctypes.c_float(scale), None)
+
+    assert run(P=0) == 1 and run(P=65) == 1 and run(S=510) == 1  # S % P != 0
+    assert run(D=96) == 2
+    assert run(Hq=3) == 1 and run(scale=0.0) == 1 and run(q=0) == 1
+    assert run(ws=FAKE + 16) == 1  # workspace not 256-byte aligned
+    assert run(ws_bytes=1024) == 1  # workspace too small
     assert run(S=0) == 0

@@ -380,6 +380,41 @@ def test_attn_bwd_against_oracle(sa, shape):
         assert worst <= 1.0, f"{name}: error exceeds its bound by {worst:.2f}x"
 
 
+@pytest.mark.parametrize("P", [1, 4])
+def test_ring_host_matches_device_ring(sa, P):
+    """attn_ring_fwd_host (host buffers in and out) gives bitwise the device-side
+    ring (one attn_partial per chunk, then lse_merge; P = 1: attn_fwd) and the
+    oracle's values within the tolerance, from pinned or pageable inputs, and
+    the same again from four calls queued on two alternating (stream,
+    workspace) sets without waiting in between."""
+    B, Hq, Hkv, S, D = 1, 4, 2, 512, 128
+    q, k, v = workloads.make_qkv(adhoc(B, Hq, Hkv, S, D, True, seed=81))
+    qp, kp, vp = (t.pin_memory() for t in (q, k, v))
+    o_h, lse_h = sa.ring_attn_fwd_host(qp, kp, vp, P, causal=True)
+    qd, kd, vd = to_dev(q, k, v)
+    if P == 1:
+        o_d, lse_d = sa.attn_fwd(qd, kd, vd, causal=True)
+    else:
+        o_d, lse_d = sa.ring_attn_fwd(qd, kd, vd, P=P, causal=True, grouped=False)
+    assert torch.equal(o_h, o_d.cpu()) and torch.equal(lse_h, lse_d.cpu())
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=True)
+    check_o(o_h, o_ref)
+    check_lse(lse_h, lse_ref)
+    o2, l2 = sa.ring_attn_fwd_host(q, k, v, P, causal=True)  # pageable
+    assert torch.equal(o2, o_h) and torch.equal(l2, lse_h)
+    need = sa.ring_host_workspace_bytes(B, Hq, Hkv, S, D, P)
+    sets = [(torch.cuda.Stream(), torch.empty(need, dtype=torch.uint8, device="cuda")) for _ in range(2)]
+    outs = []
+    for i in range(4):
+        stream, ws = sets[i % 2]
+        with torch.cuda.stream(stream):
+            outs.append(sa.ring_attn_fwd_host(qp, kp, vp, P, causal=True, workspace=ws, synchronize=False))
+    torch.cuda.synchronize()
+    for o_i, l_i in outs:
+        assert torch.equal(o_i, o_h) and torch.equal(l_i, lse_h)
+    sa.query_device_error()
+
+
 def test_attn_bwd_full_size_gqa(sa):
     """The backward at the full size of the GQA workload, in the configuration
     bench.py --backward times (the GPU forward's O and lse as its inputs): on 8

@@ -239,25 +239,27 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int):
     launches_per_step = (2 if grouped else P + 1) if P > 1 else 1
     chunk_blocks = [(0, j * C, 0, 0, j * C, S, C, j) for j in range(P)]
 
-    def step(qq, kk, vv, ev=None):
+    def step(qq, kk, vv, ev=None, oo=None, ll=None):
+        oo = o if oo is None else oo
+        ll = lse if ll is None else ll
         if fp8:  # qq, kk, vv: e4m3 Q, K and V^T
             if ev:
                 ev[0].record(stream)
-            sa.attn_fwd_fp8(qq, kk, vv, sc[0], sc[1], sc[2], causal=w.causal, out=o, lse=lse)
+            sa.attn_fwd_fp8(qq, kk, vv, sc[0], sc[1], sc[2], causal=w.causal, out=oo, lse=ll)
             if ev:
                 ev[1].record(stream)
             return
         if w.varlen:  # packed sequences: [Hq, total, D] views of the B = 1 tensors
             if ev:
                 ev[0].record(stream)
-            sa.attn_fwd_varlen(qq[0], kk[0], vv[0], cu, cu, causal=w.causal, out=o[0], lse=lse[0])
+            sa.attn_fwd_varlen(qq[0], kk[0], vv[0], cu, cu, causal=w.causal, out=oo[0], lse=ll[0])
             if ev:
                 ev[1].record(stream)
             return
         if P == 1:
             if ev:
                 ev[0].record(stream)
-            sa.attn_fwd(qq, kk, vv, causal=w.causal, out=o, lse=lse)
+            sa.attn_fwd(qq, kk, vv, causal=w.causal, out=oo, lse=ll)
             if ev:
                 ev[1].record(stream)
             return
@@ -313,37 +315,29 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int):
     e2e = None
     if rank == 0 and not args.no_e2e and not fp8 and not w.varlen:
         e2e = e2e_host_ring(sa, w, dev, stream, q_h, k_h, v_h, F, args.steps)
-    elif rank == 0 and not args.no_e2e:
+    elif rank == 0 and not args.no_e2e:  # fp8 and varlen: torch copies around the device step
         q_p, k_p, v_p = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
-        o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-        lse_host = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-        qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        sets = [{"stream": torch.cuda.Stream(dev), "in": [torch.empty_like(t) for t in (q, k, v)],
+                 "out": [torch.empty_like(o), torch.empty_like(lse)],
+                 "host": [torch.empty(o.shape, dtype=o.dtype).pin_memory(),
+                          torch.empty(lse.shape, dtype=lse.dtype).pin_memory()]} for _ in range(2)]
 
-        def e2e_step():
-            qd.copy_(q_p, non_blocking=True)
-            kd.copy_(k_p, non_blocking=True)
-            vd.copy_(v_p, non_blocking=True)
-            step(qd, kd, vd)
-            o_host.copy_(o, non_blocking=True)
-            lse_host.copy_(lse, non_blocking=True)
+        def e2e_step(st_):
+            with torch.cuda.stream(st_["stream"]):
+                for d_, h_ in zip(st_["in"], (q_p, k_p, v_p)):
+                    d_.copy_(h_, non_blocking=True)
+                step(*st_["in"], oo=st_["out"][0], ll=st_["out"][1])
+                for h_, d_ in zip(st_["host"], st_["out"]):
+                    h_.copy_(d_, non_blocking=True)
 
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize(dev)
-        n_e2e = max(3, min(args.steps, 20))
-        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
-        b_.record(stream)
-        torch.cuda.synchronize(dev)
-        e2e_ms = a.elapsed_time(b_) / n_e2e
+        e2e_ms = overlapped_steps_ms(dev, stream, sets, e2e_step, args.steps)
         h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h))
         d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
         e2e = {"value": F / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "path": "torch copies of the inputs and outputs around the device-side step, one stream"}
-        del qd, kd, vd
+               "path": ("torch copies of the inputs and outputs around the device-side step; two (stream, "
+                        "buffers) sets alternate across steps")}
+        del sets
 
     peaks, peak_src = load_peaks()
     n_attn = P if P > 1 and not grouped else 1  # attention launches per step
@@ -381,6 +375,29 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int):
     }
 
 
+def overlapped_steps_ms(dev, stream, sets, run, steps: int) -> float:
+    """Milliseconds per end-to-end step with two sets of buffers, each with its
+    own stream (set["stream"]), used alternately so that one step's copies
+    overlap its neighbours' compute: run(set) queues a whole step (uploads,
+    compute, downloads) on set["stream"]. Timed from an event before the first
+    step to one after both streams' last step."""
+    for i in range(4):
+        run(sets[i % 2])
+    torch.cuda.synchronize(dev)
+    n = max(4, min(steps, 20))
+    a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for s_ in sets:
+        s_["stream"].wait_stream(stream)
+    for i in range(n):
+        run(sets[i % 2])
+    for s_ in sets:
+        stream.wait_stream(s_["stream"])
+    b_.record(stream)
+    torch.cuda.synchronize(dev)
+    return a.elapsed_time(b_) / n
+
+
 def e2e_host_ring(sa, w: workloads.Workload, dev, stream, q_h, k_h, v_h, F: float, steps: int) -> dict:
     """The step end to end through the C ABI's host-buffer entry point
     (attn_ring_fwd_host): pinned host Q, K, V in, host O and lse out, every
@@ -390,34 +407,19 @@ def e2e_host_ring(sa, w: workloads.Workload, dev, stream, q_h, k_h, v_h, F: floa
     qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
     B, Hq, S, D, P = w.B, w.Hq, w.S, w.D, w.P
     need = sa.ring_host_workspace_bytes(B, Hq, w.Hkv, S, D, P)
-    sets = [(torch.cuda.Stream(dev), torch.empty(need, dtype=torch.uint8, device=dev),
-             torch.empty(q_h.shape, dtype=torch.bfloat16).pin_memory(),
-             torch.empty((B, Hq, S), dtype=torch.float32).pin_memory()) for _ in range(2)]
+    sets = [{"stream": torch.cuda.Stream(dev), "ws": torch.empty(need, dtype=torch.uint8, device=dev),
+             "o": torch.empty(q_h.shape, dtype=torch.bfloat16).pin_memory(),
+             "lse": torch.empty((B, Hq, S), dtype=torch.float32).pin_memory()} for _ in range(2)]
 
-    def host_step(i):
-        s_, ws, oh, lh = sets[i % 2]
-        with torch.cuda.stream(s_):
-            sa.ring_attn_fwd_host(qp, kp, vp, P, causal=w.causal, out=oh, lse=lh, workspace=ws, device=dev,
-                                  synchronize=False)
+    def host_step(st_):
+        with torch.cuda.stream(st_["stream"]):
+            sa.ring_attn_fwd_host(qp, kp, vp, P, causal=w.causal, out=st_["o"], lse=st_["lse"],
+                                  workspace=st_["ws"], device=dev, synchronize=False)
 
-    for i in range(4):
-        host_step(i)
-    torch.cuda.synchronize(dev)
-    n = max(4, min(steps, 20))
-    a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for s_, *_ in sets:
-        s_.wait_stream(stream)
-    for i in range(n):
-        host_step(i)
-    for s_, *_ in sets:
-        stream.wait_stream(s_)
-    b_.record(stream)
-    torch.cuda.synchronize(dev)
-    ms = a.elapsed_time(b_) / n
+    ms = overlapped_steps_ms(dev, stream, sets, host_step, steps)
     return {"value": F / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
             "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h)),
-            "d2h_bytes_per_step": sets[0][2].numel() * 2 + sets[0][3].numel() * 4,
+            "d2h_bytes_per_step": sets[0]["o"].numel() * 2 + sets[0]["lse"].numel() * 4,
             "path": ("attn_ring_fwd_host (C ABI, host buffers): Q and each K/V chunk uploaded on the library's "
                      "copy stream while earlier chunks' partials run (one attn_partial per chunk), merge, O and "
                      "lse downloaded; two (stream, workspace) sets alternate across steps")}
@@ -442,8 +444,9 @@ def run_ours_backward(args, w: workloads.Workload, rank: int, world: int):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     delta = torch.empty_like(lse)
 
-    def step(qq, kk, vv, oo, ll, dd):
-        sa.attn_bwd(qq, kk, vv, oo, ll, dd, causal=w.causal, dq=dq, dk=dk, dv=dv, delta=delta)
+    def step(qq, kk, vv, oo, ll, dd, grads=None):
+        g_ = grads or (dq, dk, dv, delta)
+        sa.attn_bwd(qq, kk, vv, oo, ll, dd, causal=w.causal, dq=g_[0], dk=g_[1], dv=g_[2], delta=g_[3])
 
     F = 2.5 * w.attention_flops()
     sampler = ClockSampler(dev.index) if rank == 0 else None
@@ -478,31 +481,25 @@ def run_ours_backward(args, w: workloads.Workload, rank: int, world: int):
     e2e = None
     if rank == 0 and not args.no_e2e:  # pinned host Q, K, V, O, lse, dO in; dQ, dK, dV out
         ins_h = [t.pin_memory() for t in (q_h, k_h, v_h, o.cpu(), lse.cpu(), do_h)]
-        ins_d = [torch.empty_like(t, device=dev) for t in ins_h]
-        outs_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
+        sets = [{"stream": torch.cuda.Stream(dev), "in": [torch.empty_like(t, device=dev) for t in ins_h],
+                 "grads": [torch.empty_like(t) for t in (dq, dk, dv, delta)],
+                 "host": [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]}
+                for _ in range(2)]
 
-        def e2e_step():
-            for d_, h_ in zip(ins_d, ins_h):
-                d_.copy_(h_, non_blocking=True)
-            step(*ins_d)
-            for h_, d_ in zip(outs_h, (dq, dk, dv)):
-                h_.copy_(d_, non_blocking=True)
+        def e2e_step(st_):
+            with torch.cuda.stream(st_["stream"]):
+                for d_, h_ in zip(st_["in"], ins_h):
+                    d_.copy_(h_, non_blocking=True)
+                step(*st_["in"], grads=st_["grads"])
+                for h_, d_ in zip(st_["host"], st_["grads"][:3]):
+                    h_.copy_(d_, non_blocking=True)
 
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize(dev)
-        n_e2e = max(3, min(args.steps, 20))
-        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
-        b_.record(stream)
-        torch.cuda.synchronize(dev)
-        e2e_ms = a.elapsed_time(b_) / n_e2e
+        e2e_ms = overlapped_steps_ms(dev, stream, sets, e2e_step, args.steps)
         e2e = {"value": F / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in ins_h),
-               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in outs_h)}
-        del ins_d
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in sets[0]["host"]),
+               "path": ("torch copies around attn_bwd; two (stream, buffers) sets alternate across steps")}
+        del sets
 
     peaks, peak_src = load_peaks()
     achieved = F / (call_ms * 1e-3) / 1e12

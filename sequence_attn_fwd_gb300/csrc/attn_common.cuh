@@ -338,12 +338,13 @@ __device__ __forceinline__ bool softmax_row(const AttnParams &p, const BlockDesc
           }
         }
         const uint32_t buf = store.stage;
-        if (c > 0) {
-          // the previous chunk's box must have been read out of the buffer
-          if (leader) bulk_wait_group_read<0>();
-          __syncwarp();
-          named_bar_sync(store.named_bar, 128);
-        }
+        // the previous box stored from this buffer (the previous chunk's, or
+        // the last one of this warpgroup's previous tile) must have been read
+        // out of it; waiting here rather than after each tile's last store
+        // keeps that read off the path to the next tile's softmax
+        if (leader) bulk_wait_group_read<0>();
+        __syncwarp();
+        named_bar_sync(store.named_bar, 128);
         const uint32_t dst = buf + row_in_tile * 128u;
 #pragma unroll
         for (int k = 0; k < 8; ++k)
@@ -358,9 +359,9 @@ __device__ __forceinline__ bool softmax_row(const AttnParams &p, const BlockDesc
           bulk_commit_group();
         }
       }
-      // The staging box is reused by the next tile and freed when the CTA
-      // exits: the last store must have read it.
-      if (leader) bulk_wait_group_read<0>();
+      // The last store may still be reading the buffer: the next tile's first
+      // chunk waits for it, and the caller waits for every store before the
+      // CTA exits.
       if (row_valid) p.lse[row_index] = (l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
       return true;  // every thread of the warpgroup had the final O
     }

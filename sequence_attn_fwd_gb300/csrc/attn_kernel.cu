@@ -379,6 +379,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++u;
       if (!ok) break;  // the same on every thread of the warpgroup
     }
+    // the epilogue's last TMA stores: read out of shared memory and written
+    // to global memory before the CTA's shared memory goes away
+    if ((threadIdx.x & 127) == 0) bulk_wait_all();
   }
 
   tc_fence_before();

@@ -25,6 +25,7 @@ of all ranks / max-over-ranks time.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -678,12 +679,19 @@ def main(argv=None):
     ap.add_argument("--backward", action="store_true",
                     help="time the backward (attn_bwd: dQ, dK, dV) instead of the forward step "
                          "(single-pass workloads)")
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="with --backward: a smaller sequence length of the same workload (profiling the "
+                         "same kernels on a small case)")
     ap.add_argument("--ring-schedule", action="store_true",
                     help="instead of the step: per-hop device times of the emulated causal ring, "
                          "contiguous vs zigzag layout (ring workloads)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
     w = workloads.WORKLOADS[args.workload]
+    if args.seq_len is not None:
+        if not args.backward or w.P > 1 or w.varlen or args.seq_len < 1:
+            raise SystemExit("--seq-len applies to --backward on single-pass workloads")
+        w = dataclasses.replace(w, S=args.seq_len, name=f"{w.name}@S{args.seq_len}")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

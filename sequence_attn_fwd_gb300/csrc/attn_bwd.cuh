@@ -43,8 +43,9 @@ constexpr int kThreads = 576;
 constexpr int kMmaWarp = 16, kTmaWarp = 17;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// barriers: stay_full, full[S], empty[S], st_full[2], pt_full[2], acc_done
-constexpr int kNumBarriers = 1 + 2 * kStages + 5;
+// barriers: stay_full, full[S], empty[S / 2] (one per iteration's pair of
+// slots), st_full[2], pt_full[2], acc_done
+constexpr int kNumBarriers = 1 + kStages + kStages / 2 + 5;
 constexpr int kSmemBytes = 1024 + 2 * kTileBytes + kStages * kTileBytes + 2 * 2 * kRows * 4 +
                            8 * kNumBarriers + 16;
 
@@ -158,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   const uint32_t bar0 = smem_addr(bars);
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
-  const int kBarStay = 0, kBarFull = 1, kBarEmpty = 1 + kStages, kBarSt = 1 + 2 * kStages,
+  const int kBarStay = 0, kBarFull = 1, kBarEmpty = 1 + kStages, kBarSt = kBarEmpty + kStages / 2,
             kBarPt = kBarSt + 2, kBarAcc = kBarPt + 2;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -188,10 +189,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarStay), 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(kBarFull + s), 1);
-      mbar_init(bar(kBarEmpty + s), 1);
-    }
+    for (int s = 0; s < kStages; ++s) mbar_init(bar(kBarFull + s), 1);
+    for (int s = 0; s < kStages / 2; ++s) mbar_init(bar(kBarEmpty + s), 1);
     for (int h = 0; h < 2; ++h) {
       mbar_init(bar(kBarSt + h), 1);
       mbar_init(bar(kBarPt + h), 8);  // one arrival per warp of the two warpgroups of half h
@@ -233,12 +232,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = 0; it < n_iter && ok; ++it) {
         int row, q_head;
         stream_of(it, row, q_head);
+        // both slots of iteration it are free once iteration it - kStages / 2 is released
+        const int pair = it % (kStages / 2), round = it / (kStages / 2);
+        if (round > 0 && !mbar_wait(bar(kBarEmpty + pair), (round - 1) & 1, abort_flag, err)) break;
         for (int which = 0; which < 2; ++which, ++c) {  // Q_i then dO_i, or K_j then V_j
           const int slot = c % kStages;
-          if (c >= kStages && !mbar_wait(bar(kBarEmpty + slot), ((c / kStages) - 1) & 1, abort_flag, err)) {
-            ok = false;
-            break;
-          }
           mbar_arrive_expect_tx(bar(kBarFull + slot), kTileBytes);
           const CUtensorMap *map = kDq ? (which ? &tm_v : &tm_k) : (which ? &tm_do : &tm_q);
           load_tile(smem_addr(sRing + slot * kTileBytes), map, bar(kBarFull + slot), row,
@@ -259,12 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // accumulation is issued once its warpgroup is done, followed by the
       // next iteration's scores of the same half, so one warpgroup's
       // element-wise pass overlaps the other half's MMAs.
-      auto wait_full = [&](int it) {
+      auto full = [&](int it) {  // both tiles of iteration it have landed (no fence)
         const int c0 = 2 * it, c1 = 2 * it + 1;
-        const bool got = mbar_wait(bar(kBarFull + c0 % kStages), (c0 / kStages) & 1, abort_flag, err) &&
-                         mbar_wait(bar(kBarFull + c1 % kStages), (c1 / kStages) & 1, abort_flag, err);
-        tc_fence_after();
-        return got;
+        return mbar_wait(bar(kBarFull + c0 % kStages), (c0 / kStages) & 1, abort_flag, err) &&
+               mbar_wait(bar(kBarFull + c1 % kStages), (c1 / kStages) & 1, abort_flag, err);
       };
       auto ring0 = [&](int it) { return ring + ((2 * it) % kStages) * kTileBytes; };
       auto ring1 = [&](int it) { return ring + ((2 * it + 1) % kStages) * kTileBytes; };
@@ -281,25 +277,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_acc_tmem(tAcc1, tDP, ring0(it), h, it == 0 && h == 0);  // dK += dS^T Q_i
         }
       };
-      bool ok = mbar_wait(bar(kBarStay), 0, abort_flag, err) && wait_full(0);
+      // The issuing thread's waits, commits and fences stall the tensor pipe
+      // once its short queue drains, so they are gathered: one fence after
+      // the element-wise wait and the next tiles' arrival, then the half's
+      // accumulation and the next scores as one burst; one commit releases
+      // both ring slots of an iteration.
+      bool ok = mbar_wait(bar(kBarStay), 0, abort_flag, err) && full(0);
+      tc_fence_after();
       if (ok) {
         scores(0, 0);
         scores(0, 1);
       }
       for (int it = 0; ok && it < n_iter; ++it) {
         const bool more = it + 1 < n_iter;
-        if (!mbar_wait(bar(kBarPt), it & 1, abort_flag, err)) break;
+        if (!mbar_wait(bar(kBarPt), it & 1, abort_flag, err) || (more && !full(it + 1))) break;
         tc_fence_after();
         accumulate(it, 0);
-        if (more) {
-          if (!wait_full(it + 1)) break;
-          scores(it + 1, 0);
-        }
+        if (more) scores(it + 1, 0);
         if (!mbar_wait(bar(kBarPt + 1), it & 1, abort_flag, err)) break;
         tc_fence_after();
         accumulate(it, 1);
-        mma_commit(bar(kBarEmpty + (2 * it) % kStages));
-        mma_commit(bar(kBarEmpty + (2 * it + 1) % kStages));
+        mma_commit(bar(kBarEmpty + it % (kStages / 2)));
         if (more) scores(it + 1, 1);
       }
       mma_commit(bar(kBarAcc));

@@ -73,7 +73,7 @@ bool make_out_map(CUtensorMap *map, void *base, int D, long long rows, long long
                         static_cast<cuuint64_t>(heads)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * es,
                            static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(D) * es};
-  cuuint32_t box[3] = {128u / es, 128u, 1u};
+  cuuint32_t box[3] = {128u / es, 32u, 1u};  // 128 bytes x the 32 rows of one warp
   cuuint32_t estride[3] = {1u, 1u, 1u};
   return fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base,
             dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

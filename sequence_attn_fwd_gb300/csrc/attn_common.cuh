@@ -310,11 +310,16 @@ __device__ __forceinline__ bool softmax_row(const AttnParams &p, const BlockDesc
       via_tma = named_bar_and(store.named_bar, 128, have_o) && !keep_rows && box_fits;
     }
     if (via_tma) {
+      // Each warp stores its own 32 rows from its own quarter of the
+      // warpgroup's staging buffer (4 KB), so only warp-level syncs are needed
+      // between writing the buffer and the TMA store that reads it.
       constexpr int kChunkCols = kF32Out ? 32 : 64;  // 128 bytes of a row
       constexpr int kChunks = D / kChunkCols;
-      const bool leader = (threadIdx.x & 127) == 0;
+      const bool wleader = (threadIdx.x & 31) == 0;
       const uint32_t row_in_tile = static_cast<uint32_t>(row - tile_first_row);
+      const uint32_t warp_row0 = row_in_tile & ~31u;
       const uint32_t swz = row_in_tile & 7u;
+      const uint32_t wbuf = store.stage + warp_row0 * 128u;
 #pragma unroll 1
       for (int c = 0; c < kChunks; ++c) {
         uint32_t v[32];
@@ -337,30 +342,27 @@ __device__ __forceinline__ bool softmax_row(const AttnParams &p, const BlockDesc
             }
           }
         }
-        const uint32_t buf = store.stage;
-        // the previous box stored from this buffer (the previous chunk's, or
-        // the last one of this warpgroup's previous tile) must have been read
+        // the previous box this warp stored from its quarter (the previous
+        // chunk's, or the last one of its previous tile) must have been read
         // out of it; waiting here rather than after each tile's last store
         // keeps that read off the path to the next tile's softmax
-        if (leader) bulk_wait_group_read<0>();
+        if (wleader) bulk_wait_group_read<0>();
         __syncwarp();
-        named_bar_sync(store.named_bar, 128);
-        const uint32_t dst = buf + row_in_tile * 128u;
+        const uint32_t dst = wbuf + (row_in_tile & 31u) * 128u;
 #pragma unroll
         for (int k = 0; k < 8; ++k)
           st_shared_v4(dst + ((static_cast<uint32_t>(k) ^ swz) << 4), v[4 * k], v[4 * k + 1],
                        v[4 * k + 2], v[4 * k + 3]);
         fence_proxy_async_shared();
         __syncwarp();
-        named_bar_sync(store.named_bar, 128);
-        if (leader) {
-          tma_store_3d(store.map, buf, c * kChunkCols, static_cast<int>(blk.o_row + tile_first_row),
-                       store.head);
+        if (wleader) {
+          tma_store_3d(store.map, wbuf, c * kChunkCols,
+                       static_cast<int>(blk.o_row + tile_first_row + warp_row0), store.head);
           bulk_commit_group();
         }
       }
-      // The last store may still be reading the buffer: the next tile's first
-      // chunk waits for it, and the caller waits for every store before the
+      // The last stores may still be reading the buffer: the next tile's first
+      // chunk waits for them, and the caller waits for every store before the
       // CTA exits.
       if (row_valid) p.lse[row_index] = (l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
       return true;  // every thread of the warpgroup had the final O

@@ -379,9 +379,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++u;
       if (!ok) break;  // the same on every thread of the warpgroup
     }
-    // the epilogue's last TMA stores: read out of shared memory and written
-    // to global memory before the CTA's shared memory goes away
-    if ((threadIdx.x & 127) == 0) bulk_wait_all();
+    // the epilogue's last TMA stores (issued by lane 0 of each warp): read out
+    // of shared memory and written to global memory before the CTA's shared
+    // memory goes away
+    if (lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();

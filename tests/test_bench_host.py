@@ -139,3 +139,13 @@ def test_backward_sample_counts_two_and_a_half_forward_flops():
     rate, secs, calls, _ = bench.oracle_backward_sample(w, 0.0, prefix=32)
     assert calls == 1
     assert rate * 1e12 * secs == pytest.approx(2.5 * 4 * w.D * 32 * 33 / 2, rel=1e-9)
+
+
+def test_seq_len_override_is_backward_only():
+    """--seq-len (a small case of a workload's backward for profiling) is refused
+    for the forward and for ring workloads."""
+    for argv in (["--seq-len", "4096"],
+                 ["--seq-len", "4096", "--backward", "--workload", "ring8_b2h32s4096d128_causal"],
+                 ["--seq-len", "0", "--backward", "--workload", "gqa_b1hq28hkv4s32768d128_causal"]):
+        with pytest.raises(SystemExit):
+            bench.main(argv)

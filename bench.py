@@ -106,14 +106,26 @@ KERNEL_SOURCES = {
 }
 
 
+def code_text(source: str) -> str:
+    """C/CUDA source without comments and with runs of whitespace collapsed,
+    so that an edit to comments alone leaves a kernel's digest unchanged (the
+    sources hold no string literal with comment markers in it)."""
+    import re
+
+    source = re.sub(r"/\*.*?\*/", " ", source, flags=re.S)
+    source = re.sub(r"//[^\n]*", " ", source)
+    return " ".join(source.split())
+
+
 def sources_digest(kernel: str) -> str:
-    """SHA-256 prefix of the sources a kernel is built from."""
+    """SHA-256 prefix of the code (comments left out) of the sources a kernel
+    is built from."""
     import hashlib
 
     m = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "sequence_attn_fwd_gb300", "csrc", f), "rb") as fh:
-            m.update(fh.read())
+        with open(os.path.join(ROOT, "sequence_attn_fwd_gb300", "csrc", f), encoding="utf-8") as fh:
+            m.update(code_text(fh.read()).encode("utf-8"))
     return m.hexdigest()[:16]
 
 

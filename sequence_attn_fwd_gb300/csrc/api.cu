@@ -63,7 +63,8 @@ bool make_map(CUtensorMap *map, const void *base, int D, long long rows, long lo
 }
 
 // 3-D view [heads][rows][D] of the output (fp32 or bf16, rows contiguous per
-// head); box 128 bytes x 128 rows x 1 with 128-byte swizzle, for TMA stores.
+// head); box 128 bytes x 32 rows x 1 (the rows of one warp) with 128-byte
+// swizzle, for TMA stores.
 bool make_out_map(CUtensorMap *map, void *base, int D, long long rows, long long heads,
                   bool f32) {
   EncodeTiledFn fn = encode_fn();

@@ -168,13 +168,14 @@ __device__ __forceinline__ void write_empty_rows(const AttnParams &p, const Bloc
 
 // How a warpgroup's epilogue writes its 128-row O tile. With a tensor map the
 // tile leaves through shared memory: each thread puts its row's 128-byte slice
-// of a column chunk into a 128-byte-swizzled staging box (conflict-free), and
-// one thread stores the box with TMA, so global writes are whole lines instead
-// of one 16-byte piece of 32 different rows per warp store. Without a map each
-// thread stores its own row.
+// of a column chunk into its warp's quarter of a 128-byte-swizzled staging
+// buffer (conflict-free), and lane 0 of the warp stores that quarter (32 rows)
+// with TMA, so global writes are whole lines instead of one 16-byte piece of
+// 32 different rows per warp store. Without a map each thread stores its own
+// row.
 struct EpilogueStore {
-  const CUtensorMap *map;  // O as [heads][rows][D], box 128 bytes x 128 rows x 1, 128-byte swizzle
-  uint32_t stage;          // shared address of this warpgroup's 16 KB staging box (1024-byte aligned)
+  const CUtensorMap *map;  // O as [heads][rows][D], box 128 bytes x 32 rows x 1, 128-byte swizzle
+  uint32_t stage;          // shared address of this warpgroup's 16 KB staging buffer (1024-byte aligned)
   int named_bar;           // barrier id private to the warpgroup (128 threads)
   int head;                // third map coordinate, b * Hq + hq
 };

@@ -50,7 +50,8 @@ bool attention_uses_pair(int D);
 
 // Tensor maps are 3-D views [heads][rows][D] built by the caller: q, k, v of
 // bf16 data, box 64 columns x rows x 1; o of the output type (fp32 when
-// f32_out, else bf16), box 128 bytes x 128 rows x 1; all with 128-byte swizzle.
+// f32_out, else bf16), box 128 bytes x 32 rows x 1 (one warp's rows); all with
+// 128-byte swizzle.
 cudaError_t launch_attention(int D, bool f32_out, bool pair, const CUtensorMap &tm_q,
                              const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                              const CUtensorMap &tm_o, const AttnParams &p, cudaStream_t stream);

@@ -116,6 +116,13 @@ def test_measured_traffic_follows_the_kernel_sources(tmp_path):
     assert bench.measured_traffic("attn_partial", "wl", str(tmp_path)) is None
 
 
+def test_code_text_ignores_comments_only():
+    a = "int x = 1; // one\n/* block\n comment */ int y =  2;\n"
+    b = "int x = 1;\n int y = 2; // two\n"
+    assert bench.code_text(a) == bench.code_text(b) == "int x = 1; int y = 2;"
+    assert bench.code_text("int x = 1;") != bench.code_text("int x = 2;")
+
+
 def test_ring_time_from_hops():
     r = bench.ring_time_from_hops([[1.0, 3.0], [2.0, 2.0]])
     assert r["ring_ms"] == 5.0 and r["device_ms_total"] == 8.0

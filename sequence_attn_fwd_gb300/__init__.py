@@ -483,6 +483,9 @@ def ring_attn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int
              and out.is_contiguous(), "out must be a contiguous bf16 CPU tensor shaped like q")
     _require(lse.device.type == "cpu" and lse.dtype == torch.float32 and lse.shape == (B, Hq, S)
              and lse.is_contiguous(), "lse must be a contiguous fp32 CPU tensor [B, Hq, S]")
+    if B == 0 or S == 0:  # nothing to compute (the C call would return at once)
+        _require(P >= 1 and (S == 0 or S % P == 0), "S must be a multiple of P")
+        return out, lse
     need = ring_host_workspace_bytes(B, Hq, Hkv, S, D, P)
     if workspace is None:
         # the library's copy stream writes the workspace, which torch's allocator

@@ -415,6 +415,21 @@ def test_ring_host_matches_device_ring(sa, P):
     sa.query_device_error()
 
 
+def test_ring_host_full_size_ring8(sa):
+    """The host-buffer ring at the bench's default size: bitwise the device-side
+    grouped ring (the partials of one launch per chunk and of one grouped launch
+    are bitwise equal), and empty inputs return empty outputs."""
+    w = workloads.WORKLOADS["ring8_b2h32s4096d128_causal"]
+    q, k, v = workloads.make_qkv(w)
+    o_h, lse_h = sa.ring_attn_fwd_host(q.pin_memory(), k.pin_memory(), v.pin_memory(), w.P, causal=True)
+    o_d, lse_d = sa.ring_attn_fwd(*to_dev(q, k, v), P=w.P, causal=True, grouped=True)
+    assert torch.equal(o_h, o_d.cpu()) and torch.equal(lse_h, lse_d.cpu())
+    e = torch.empty((1, 2, 0, 128), dtype=torch.bfloat16)
+    o_e, lse_e = sa.ring_attn_fwd_host(e, e, e, 4, causal=True)
+    assert o_e.shape == (1, 2, 0, 128) and lse_e.shape == (1, 2, 0)
+    sa.query_device_error()
+
+
 def test_attn_bwd_full_size_gqa(sa):
     """The backward at the full size of the GQA workload, in the configuration
     bench.py --backward times (the GPU forward's O and lse as its inputs): on 8

@@ -11,6 +11,9 @@ to, and a missing library is an error.
     o, lse = lse_merge(o_parts, lse_parts)
     o, lse = ring_attn_fwd(q, k, v, P=8, causal=True)   # P chunks + merge on one GPU
     o, lse = attn_fwd_varlen(q, k, v, cu_seqlens, cu_seqlens, causal=True)  # packed sequences
+    o, lse = attn_fwd_fp8(q8, k8, vt8, q_scale, k_scale, v_scale, causal=True)  # e4m3 inputs
+    dq, dk, dv = attn_bwd(q, k, v, o, lse, dout, causal=True)   # gradients
+    o_h, lse_h = ring_attn_fwd_host(q_h, k_h, v_h, P=8, causal=True)  # host tensors in and out
 """
 from __future__ import annotations
 

@@ -136,3 +136,26 @@ def bwd_ratio(got: torch.Tensor, ref: np.ndarray, bound: np.ndarray) -> float:
     if not np.isfinite(g).all():
         return float("inf")
     return float((np.abs(g - ref) / (bound + 2.0 ** -8 * np.abs(ref) + 1e-4)).max())
+
+
+def fp8_bound(qd, kd, vd, causal, scale):
+    """Per-element bound on |O_fp8 - O_exact| for inputs already on the e4m3
+    grid (numpy fp64, small shapes): P is rounded to e4m3 in the kernel, so
+    |dP| <= 2^-4 P (normal range) or 2^-10 (below 2^-6) in units where the row
+    maximum is >= 1 (the kernel's reference maximum never exceeds the true one),
+    and |dO_d| <= (2^-4 sum_j P_j |v_jd| + 2^-10 sum_{P_j < 2^-6} |v_jd|) / l;
+    plus the bf16 rounding of O."""
+    q, k, v = (t.double().numpy() for t in (qd, kd, vd))
+    B, Hq, S, D = q.shape
+    g = Hq // k.shape[1]
+    bound = np.empty((B, Hq, S, D))
+    for b in range(B):
+        for h in range(Hq):
+            s = scale * q[b, h] @ k[b, h // g].T
+            if causal:
+                s = np.where(np.tril(np.ones((S, S), dtype=bool)), s, -np.inf)
+            p = np.exp(s - s.max(axis=1, keepdims=True))
+            l = p.sum(axis=1, keepdims=True)
+            av = np.abs(v[b, h // g])
+            bound[b, h] = (2.0 ** -4 * (p @ av) + 2.0 ** -10 * ((p < 2.0 ** -6) @ av)) / l
+    return bound

@@ -12,7 +12,7 @@ import torch
 
 import oracle
 import workloads
-from tests.parity import LSE_TOL, O_TOL, bwd_bound, bwd_dq_rows_bound, bwd_ratio, check_lse, check_o, gather_rows
+from tests.parity import LSE_TOL, O_TOL, bwd_bound, bwd_dq_rows_bound, bwd_ratio, check_lse, check_o, fp8_bound, gather_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -302,29 +302,6 @@ def test_ring_grouped_launch_is_bitwise_the_per_chunk_launches(sa):
     o2, l2 = sa.ring_attn_fwd(q, k, v, P=4, causal=True, grouped=True)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
-
-
-def fp8_bound(qd, kd, vd, causal, scale):
-    """Per-element bound on |O_fp8 - O_exact| for inputs already on the e4m3
-    grid (numpy fp64, small shapes): P is rounded to e4m3 in the kernel, so
-    |dP| <= 2^-4 P (normal range) or 2^-10 (below 2^-6) in units where the row
-    maximum is >= 1 (the kernel's reference maximum never exceeds the true one),
-    and |dO_d| <= (2^-4 sum_j P_j |v_jd| + 2^-10 sum_{P_j < 2^-6} |v_jd|) / l;
-    plus the bf16 rounding of O."""
-    q, k, v = (t.double().numpy() for t in (qd, kd, vd))
-    B, Hq, S, D = q.shape
-    g = Hq // k.shape[1]
-    bound = np.empty((B, Hq, S, D))
-    for b in range(B):
-        for h in range(Hq):
-            s = scale * q[b, h] @ k[b, h // g].T
-            if causal:
-                s = np.where(np.tril(np.ones((S, S), dtype=bool)), s, -np.inf)
-            p = np.exp(s - s.max(axis=1, keepdims=True))
-            l = p.sum(axis=1, keepdims=True)
-            av = np.abs(v[b, h // g])
-            bound[b, h] = (2.0 ** -4 * (p @ av) + 2.0 ** -10 * ((p < 2.0 ** -6) @ av)) / l
-    return bound
 
 
 @pytest.mark.parametrize("shape", [(1, 2, 2, 512, True), (1, 4, 2, 1008, True), (2, 2, 1, 384, False)],

@@ -7,8 +7,10 @@ ring-chunked workload, the P key chunks' partials (by default one
 attn_partial_blocks launch over all P chunks, --partials per-chunk for one
 attn_partial launch per chunk; zero-copy views either way) and one lse_merge;
 for a single-pass workload, one attn_fwd. The
-default workload is the ring-chunked causal attention B=2, H=32, S=4096,
-D=128 with P=8 chunks of 512.
+default workload is the largest one that fits one GPU: ring-chunked causal
+attention at 131,072 tokens, B=1, Hq=32, Hkv=8, D=128, with P=16 key chunks
+of 8192 (about 37 GB of inputs, partials and outputs on the device). The
+other workloads are reachable with --workload.
 
 metric: causal-adjusted attention TFLOP/s, F = 4*B*Hq*S^2*D (halved when
 causal), over the step time; the JSON line also carries the dominant
@@ -45,7 +47,7 @@ import workloads  # noqa: E402
 
 METRIC = "attention fwd TFLOP/s (causal-adjusted) & % BF16 peak; lse_merge GB/s & % HBM"
 METRIC_BWD = "attention bwd TFLOP/s (causal-adjusted, 2.5x the forward's FLOPs) & % BF16 peak"
-DEFAULT_WORKLOAD = "ring8_b2h32s4096d128_causal"
+DEFAULT_WORKLOAD = "ring16_b1hq32hkv8s131072d128_causal"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129e6
 
@@ -230,6 +232,7 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
     q_h, k_h, v_h = workloads.make_qkv(w)
+    inputs = (q_h, k_h, v_h)  # the bf16 inputs, kept for the oracle's timed sample
     q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
     B, Hq, S, D, P, C = w.B, w.Hq, w.S, w.D, w.P, w.chunk
     o = torch.empty((B, Hq, S, D), dtype=torch.bfloat16, device=dev)
@@ -369,8 +372,7 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int):
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak,
                 "traffic": measured_traffic(entry, w.name),
-                "kernel": ("attn_fwd_2sm_kernel" if D == 128 and os.environ.get("SEQATTN_ATTN_KERNEL") == "2sm"
-                           and not grouped else f"attn_fwd_kernel<{D}>") + what,
+                "kernel": f"attn_fwd_kernel<{D}>" + what,
                 "peak_source": f"{peak_src} bf16 burst" + (" x 2 (nominal e4m3 / bf16 ratio)" if fp8 else ""),
                 "launch_ms": attn_avg_ms}
     merge = None
@@ -384,7 +386,7 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int):
     return {
         "value": value, "ms_per_step": ms_per_step, "e2e": e2e, "roofline": roofline, "merge": merge,
         "gpu_launches": args.steps * launches_per_step, "clocks": clocks,
-        "attn_ms_per_step": statistics.mean(attn_ms),
+        "attn_ms_per_step": statistics.mean(attn_ms), "inputs": inputs,
     }
 
 
@@ -739,7 +741,7 @@ def main(argv=None):
                    "sample": f"the oracle's backward on the first 1024 positions of {calls} "
                              f"(batch, query head) pairs in turn ({secs:.1f} s), fp64 chain rule"}
         elif world == 1 and not args.no_cpu_baseline:
-            val, secs, heads, threads = oracle_sample(w, args.cpu_baseline_budget)
+            val, secs, heads, threads = oracle_sample(w, args.cpu_baseline_budget, *r.get("inputs", ()))
             unit = "(sequence, head), sequences and heads" if w.varlen else "(batch, head), heads"
             cpu = {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                    "sample": f"{heads} seeded query rows of the workload (up to 256 per {unit} "

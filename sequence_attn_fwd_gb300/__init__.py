@@ -431,18 +431,32 @@ def ring_attn_fwd_static(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: i
     or loops that cannot afford cudaMalloc/cudaFree). Problems whose partials
     exceed the array are rejected. Calls that overlap on the GPU share the
     array and race; the first call on a device sets up the array's address.
-    Here ``out``/``lse`` are allocated through torch only when not given."""
+    Here ``out``/``lse`` are allocated through torch only when not given.
+
+    Shapes are checked before anything else (so a mismatch is refused before
+    any launch), then dtypes, layouts and devices: q bf16 [B,Hq,S,D], k/v bf16
+    [B,Hkv,S,D], out bf16 [B,Hq,S,D] and lse fp32 [B,Hq,S], all contiguous and
+    on q's device."""
     _require(q.dim() == 4 and k.dim() == 4 and v.shape == k.shape, "expected [B,H,S,D] tensors")
     B, Hq, S, D = q.shape
     Hkv = k.shape[1]
+    _require(k.shape[0] == B and k.shape[2] == S and k.shape[3] == D, "K/V shape mismatch")
+    _require(Hkv > 0 and Hq % Hkv == 0, "Hq must be a multiple of Hkv")
+    _require(out is None or tuple(out.shape) == (B, Hq, S, D), "bad out: expected [B,Hq,S,D]")
+    _require(lse is None or tuple(lse.shape) == (B, Hq, S), "bad lse: expected [B,Hq,S]")
     for t in (q, k, v):
         _require(t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous(),
                  "q, k, v must be contiguous bf16 CUDA tensors")
+        _require(t.device == q.device, "q, k, v must be on one device")
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    _require(out.dtype == torch.bfloat16 and out.is_contiguous() and out.device == q.device,
+             "bad out: must be a contiguous bf16 tensor on q's device")
+    _require(lse.dtype == torch.float32 and lse.is_contiguous() and lse.device == q.device,
+             "bad lse: must be a contiguous fp32 tensor on q's device")
     st = lib.attn_ring_fwd_static(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                                   B, Hq, Hkv, S, D, int(P), int(bool(causal)), scale, _stream_handle(q.device))
     _check(st, "attn_ring_fwd_static")

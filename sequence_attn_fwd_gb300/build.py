@@ -23,7 +23,7 @@ CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libseqattn.so")
 SOURCES = ["attn_kernel.cu", "lse_merge.cu", "api.cu"]
-HEADERS = ["ptx.cuh", "kernels.h", "attn_common.cuh", "attn_2sm.cuh", "attn_bwd.cuh"]
+HEADERS = ["ptx.cuh", "kernels.h", "attn_common.cuh", "attn_bwd.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -123,12 +123,10 @@ int run_attention(const void *q, const void *k, const void *v, long long q_off, 
     return ATTN_ERR_INVALID_ARG;
 
   CUtensorMap tq, tk, tv, to;
-  const bool pair = seqattn::attention_uses_pair(D);
   // An empty key set still needs well-formed maps; no KV tile is ever loaded.
   const long long kv_rows = Skv > 0 ? Skv : 1;
   if (!make_map(&tq, q, D, Sq, static_cast<long long>(B) * Hq, static_cast<long long>(Sq) * D) ||
-      !make_map(&tk, k, D, kv_rows, static_cast<long long>(B) * Hkv, kv_head_stride,
-                pair ? 64u : 128u) ||
+      !make_map(&tk, k, D, kv_rows, static_cast<long long>(B) * Hkv, kv_head_stride) ||
       !make_map(&tv, v, D, kv_rows, static_cast<long long>(B) * Hkv, kv_head_stride) ||
       !make_out_map(&to, o, D, Sq, static_cast<long long>(B) * Hq, f32_out))
     return cuda_fail(cudaErrorInvalidValue);
@@ -149,7 +147,7 @@ int run_attention(const void *q, const void *k, const void *v, long long q_off, 
   p.skip_empty = skip_empty ? 1 : 0;
   p.o_rows = Sq;
   p.o_scale = 1.f;
-  cudaError_t e = seqattn::launch_attention(D, f32_out, pair, tq, tk, tv, to, p, stream);
+  cudaError_t e = seqattn::launch_attention(D, f32_out, tq, tk, tv, to, p, stream);
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 

@@ -437,27 +437,13 @@ cudaError_t launch_dispatch(int D, bool f32_out, const CUtensorMap &tq, const CU
 }  // namespace
 }  // namespace seqattn
 
-#include "attn_2sm.cuh"
 #include "attn_bwd.cuh"
 
 namespace seqattn {
 
-bool attention_uses_pair(int D) {
-  // The single-SM kernel measured faster on GB300 and is the default;
-  // SEQATTN_ATTN_KERNEL=2sm selects the SM-pair kernel for head dim 128
-  // (read once per process).
-  static const bool pair = [] {
-    const char *v = getenv("SEQATTN_ATTN_KERNEL");
-    return v != nullptr && strcmp(v, "2sm") == 0;
-  }();
-  return D == 128 && pair;
-}
-
-cudaError_t launch_attention(int D, bool f32_out, bool pair, const CUtensorMap &tq,
-                             const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &to,
-                             const AttnParams &p, cudaStream_t stream) {
-  if (pair) return f32_out ? pair2sm::launch_pair<true>(tq, tk, tv, p, stream)
-                           : pair2sm::launch_pair<false>(tq, tk, tv, p, stream);
+cudaError_t launch_attention(int D, bool f32_out, const CUtensorMap &tq, const CUtensorMap &tk,
+                             const CUtensorMap &tv, const CUtensorMap &to, const AttnParams &p,
+                             cudaStream_t stream) {
   return launch_dispatch(D, f32_out, tq, tk, tv, to, p, SingleProblem{0},
                          static_cast<long long>(p.B) * p.Hq * p.n_qblocks, stream);
 }

@@ -43,18 +43,13 @@ struct BlockTable {
   BlockDesc b[kMaxLaunchBlocks];
 };
 
-// Whether attention with head dim D runs on SM pairs (2-SM MMAs). The pair
-// kernel wants the K tensor map with 64-row boxes; every other map (and every
-// map of the single-SM kernel) uses 128-row boxes.
-bool attention_uses_pair(int D);
-
 // Tensor maps are 3-D views [heads][rows][D] built by the caller: q, k, v of
-// bf16 data, box 64 columns x rows x 1; o of the output type (fp32 when
+// bf16 data, box 64 columns x 128 rows x 1; o of the output type (fp32 when
 // f32_out, else bf16), box 128 bytes x 32 rows x 1 (one warp's rows); all with
 // 128-byte swizzle.
-cudaError_t launch_attention(int D, bool f32_out, bool pair, const CUtensorMap &tm_q,
-                             const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                             const CUtensorMap &tm_o, const AttnParams &p, cudaStream_t stream);
+cudaError_t launch_attention(int D, bool f32_out, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                             const CUtensorMap &tm_v, const CUtensorMap &tm_o, const AttnParams &p,
+                             cudaStream_t stream);
 
 // Backward (head dim 128): gradients of a forward whose O and lse are given.
 struct BwdParams {

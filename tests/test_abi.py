@@ -210,3 +210,40 @@ def test_ring_host_argument_checks(lib):
     assert run(ws=FAKE + 16) == 1  # workspace not 256-byte aligned
     assert run(ws_bytes=1024) == 1  # workspace too small
     assert run(S=0) == 0
+
+
+def test_ring_static_argument_checks(lib):
+    """attn_ring_fwd_static refuses bad sizes and problems beyond its array
+    before any CUDA call."""
+    def call(B=1, Hq=4, Hkv=4, S=2048, D=128, P=16):
+        return lib.attn_ring_fwd_static(FAKE, FAKE, FAKE, FAKE, FAKE, B, Hq, Hkv, S, D, P, 1,
+                                        ctypes.c_float(0.125), None)
+
+    assert call() == 2            # 16 x 4 x 2048 x 129 x 4 bytes > 64 MiB
+    assert call(P=0) == 1
+    assert call(S=1000, P=16) == 1  # S not a multiple of P
+    assert call(D=96, S=256, P=2) == 2
+    assert call(B=0, S=256, P=2) == 0  # nothing to compute
+
+
+def test_ring_static_wrapper_refuses_bad_shapes_before_launch():
+    """The Python wrapper checks K/V and given outputs' shapes before anything
+    else, so a mismatch never reaches the library (CPU tensors here: the shape
+    checks come ahead of the device checks)."""
+    import torch
+
+    import sequence_attn_fwd_gb300 as sa
+
+    q = torch.zeros((1, 4, 256, 64), dtype=torch.bfloat16)
+    kv = torch.zeros((1, 2, 256, 64), dtype=torch.bfloat16)
+    short = torch.zeros((1, 2, 128, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="K/V shape"):
+        sa.ring_attn_fwd_static(q, short, short, P=2)
+    with pytest.raises(ValueError, match="K/V shape"):
+        sa.ring_attn_fwd_static(q, kv[..., :32], kv[..., :32], P=2)
+    with pytest.raises(ValueError, match="bad out"):
+        sa.ring_attn_fwd_static(q, kv, kv, P=2, out=torch.zeros((1, 4, 128, 64), dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="bad lse"):
+        sa.ring_attn_fwd_static(q, kv, kv, P=2, lse=torch.zeros((1, 4, 255), dtype=torch.float32))
+    with pytest.raises(ValueError, match="CUDA"):
+        sa.ring_attn_fwd_static(q, kv, kv, P=2)  # right shapes, but not on a GPU

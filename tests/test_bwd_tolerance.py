@@ -2,7 +2,9 @@
 kernels' arithmetic on the CPU: P formed in fp32 from the fp32 scores and lse
 and rounded to bf16, delta formed in fp32 from a bf16 O, dS rounded to bf16,
 fp32 products, bf16 results. The emulated gradients must lie within the bound
-of every element, and a planted error of a few percent must not."""
+of every element, and a planted error of a few percent must not. (The bound's
+error of P is derived per element from the score accumulation, the exponent
+argument's roundings, the given lse and the exponential unit: p_rel_error.)"""
 import math
 
 import numpy as np

@@ -1,19 +1,21 @@
-"""The e4m3 forward's parity bound (tests/parity.py fp8_bound) against an
-emulation of the kernel's one approximation beyond rounding on the CPU: P
-rounded to e4m3 (round to nearest even) before P V, l summed from the
-unrounded P, O rounded to bf16. The emulated O must lie within the bound of
-every element (plus the 2^-8 |O| + 1e-4 the GPU test adds) with its mean error
-below a quarter of the mean bound, the two criteria of the GPU test; O off by
-25 % or taken from the wrong head must fail them. (The worst-case bound lets
-errors of about 10 % through: it is the mean criterion that catches the
-systematic ones.)"""
+"""The e4m3 forward's parity criteria (tests/parity.py fp8_bound and
+fp8_slope_errors) against an emulation of the kernel's one approximation
+beyond rounding on the CPU: P rounded to e4m3 (round to nearest even) before
+P V, l summed from the unrounded P, O rounded to bf16. The emulated O must
+pass the three criteria of the GPU test: every element within the bound (plus
+the 2^-8 |O| + 1e-4 the GPU test adds), the mean error below a quarter of the
+mean bound, and the least-squares slopes of O on the oracle's, per head and
+per column, within 2^-7 of 1. Systematic errors must fail them: O uniformly
+3 % or 10 % too large, a V scale off by 10 %, one column off by 5 %, or O
+taken from the wrong head. The element bound alone lets a uniform error of
+about 10 % through (it is a worst case of 2^-4 per P); the slopes do not."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import workloads
-from tests.parity import fp8_bound
+from tests.parity import FP8_SLOPE_TOL, fp8_bound, fp8_slope_errors
 
 
 def e4m3_grid(t: torch.Tensor, scale: float) -> torch.Tensor:
@@ -50,8 +52,19 @@ def test_emulated_e4m3_p_lies_within_the_bound(causal):
 
     def passes(x):
         err = np.abs(x - o_ref)
-        return bool((err <= tol).all()) and err.mean() <= 0.25 * tol.mean()
+        head_dev, col_dev = fp8_slope_errors(x, o_ref)
+        return (bool((err <= tol).all()) and err.mean() <= 0.25 * tol.mean()
+                and head_dev <= FP8_SLOPE_TOL and col_dev <= FP8_SLOPE_TOL)
 
     assert passes(got)
+    # the emulated slopes sit well inside the limit
+    assert max(fp8_slope_errors(got, o_ref)) <= 0.5 * FP8_SLOPE_TOL
+    assert not passes(got * 1.03)
+    assert not passes(got * 1.10)
     assert not passes(got * 1.25)
+    # V's scale folded in wrong by 10 %: the attention of 1.1 V
+    assert not passes(emulate(qd, kd, (vd.float() * 1.1).to(torch.bfloat16), causal, w.scale))
+    one_col = got.copy()
+    one_col[..., 7] *= 1.05
+    assert not passes(one_col)
     assert not passes(np.roll(got, 1, axis=1))  # a neighbouring head's output

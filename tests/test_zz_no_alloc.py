@@ -1,4 +1,4 @@
-"""The allocation-free ring entry point against the regular one.
+"""The allocation-free ring entry point against the regular one and the oracle.
 
 attn_ring_fwd_static exists for callers that cannot allocate device memory
 themselves (a host application whose allocator already owns the device's
@@ -14,8 +14,9 @@ import math
 import pytest
 import torch
 
+import oracle
 import workloads
-from tests.parity import LSE_TOL, O_TOL
+from tests.parity import LSE_TOL, O_TOL, check_lse, check_o
 
 pytestmark = pytest.mark.gpu
 
@@ -27,24 +28,36 @@ def call_static(lib, q, k, v, o, lse, P, causal):
                                     torch.cuda.current_stream().cuda_stream)
 
 
-def test_static_scratch_ring_matches_caller_scratch_ring(cuda_dev):
+def test_static_scratch_ring_matches_caller_scratch_ring_and_oracle(cuda_dev):
+    """Calls in a row on problems that share the array: the causal call comes
+    right after a non-causal one of the same shape, so the partial rows a
+    causal chunk cannot see still hold the previous call's finite values (the
+    merge must never read them); a third call changes head dim and part count.
+    Each result equals the caller-scratch ring within the tolerance and matches
+    the oracle on every row. The last call goes through the Python wrapper."""
     import sequence_attn_fwd_gb300 as sa
 
     lib = sa.lib
-    # two different problems in a row: the second call finds the first one's
-    # partials still in the shared array
-    cases = [workloads.Workload("noalloc_a", 2, 4, 2, 1024, 128, True, 8, 2024),
-             workloads.Workload("noalloc_b", 1, 3, 3, 768, 64, False, 3, 2025)]
-    for w in cases:
-        q, k, v = (t.cuda() for t in workloads.make_qkv(w))
-        o = torch.empty_like(q)
-        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
-        assert call_static(lib, q, k, v, o, lse, w.P, w.causal) == 0
-        o_ref, lse_ref = sa.ring_attn_fwd(q, k, v, P=w.P, causal=w.causal)
+    cases = [workloads.Workload("noalloc_a_full", 2, 4, 2, 1024, 128, False, 8, 2024),
+             workloads.Workload("noalloc_a_causal", 2, 4, 2, 1024, 128, True, 8, 2024),
+             workloads.Workload("noalloc_b", 1, 3, 3, 768, 64, True, 3, 2025)]
+    for i, w in enumerate(cases):
+        q_h, k_h, v_h = workloads.make_qkv(w)
+        q, k, v = (t.cuda() for t in (q_h, k_h, v_h))
+        if i < len(cases) - 1:
+            o = torch.empty_like(q)
+            lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+            assert call_static(lib, q, k, v, o, lse, w.P, w.causal) == 0
+        else:
+            o, lse = sa.ring_attn_fwd_static(q, k, v, P=w.P, causal=w.causal)
+        o_ring, lse_ring = sa.ring_attn_fwd(q, k, v, P=w.P, causal=w.causal)
         torch.cuda.synchronize()
-        assert (o.float() - o_ref.float()).abs().max().item() <= O_TOL
-        assert torch.equal(torch.isneginf(lse), torch.isneginf(lse_ref))
-        assert (lse - lse_ref).abs().max().item() <= LSE_TOL
+        assert (o.float() - o_ring.float()).abs().max().item() <= O_TOL
+        assert torch.equal(torch.isneginf(lse), torch.isneginf(lse_ring))
+        assert (lse - lse_ring).abs().max().item() <= LSE_TOL
+        o_ref, lse_ref = oracle.attention(q_h, k_h, v_h, w.causal)
+        check_o(o, o_ref)
+        check_lse(lse, lse_ref)
     sa.query_device_error()
 
 

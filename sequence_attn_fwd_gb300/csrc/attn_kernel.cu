@@ -10,14 +10,18 @@
 // only the output). With global offsets and fp32 output the same kernel
 // produces the per-hop partial (O_i, lse_i) of Ring-Attention.
 //
-// How (one CTA = 256 query rows of one (batch, head), 320 threads):
+// How (one CTA = 256 query rows of one (batch, head), 352 threads):
 //   warp 9      TMA producer: both Q tiles once, then K_j, V_j into a ring of
 //               shared-memory slots (128-byte swizzle, 3-D tensor maps so
 //               rows past the end of a head read as zero).
-//   warp 8      MMA issuer (one thread): S_t = Q_t K_j^T into TMEM (SS form)
-//               and O_t += P_t V_j with P_t read from TMEM (TS form). The two
-//               query tiles t = 0, 1 alternate so the tensor pipe works on one
-//               tile while the other tile's softmax runs.
+//   warps 8, 10 MMA issuers, one thread each, warp 8 for query tile 0 and
+//               warp 10 for tile 1: S_t = Q_t K_j^T into TMEM (SS form) and
+//               O_t += P_t V_j with P_t read from TMEM (TS form). Their bursts
+//               alternate through a shared turn counter (tile 0, tile 1, tile
+//               0, ...), so the tensor pipe works on one tile while the other
+//               tile's softmax runs, and each issuer's barrier waits and
+//               commits overlap the other's MMAs: a lone issuer spent about
+//               40 % of every KV step in those, with the tensor pipe idle.
 //   warps 0-7   two softmax warpgroups, one per query tile, one query row per
 //               thread: load the row of S from TMEM, mask, update the running
 //               max (in log2 units), exponentiate, write P (bf16) back over S
@@ -46,9 +50,10 @@ namespace {
 
 using namespace detail;
 
-constexpr int kThreads = 320;
-constexpr int kMmaWarp = 8;
+constexpr int kThreads = 352;
+constexpr int kMmaWarp = 8;   // MMA issuer of query tile 0 (also allocates TMEM)
 constexpr int kTmaWarp = 9;
+constexpr int kMmaWarp1 = 10;  // MMA issuer of query tile 1
 
 template <int D, bool kFp8 = false>
 struct Cfg {
@@ -143,6 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(sStage + C::kSmemStage);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kNumBarriers);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  volatile int *turn = reinterpret_cast<volatile int *>(tmem_slot + 2);  // next MMA burst slot
 
   const uint32_t bar0 = smem_addr(bars);
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
@@ -157,21 +163,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQFull), 1);
-    mbar_init(bar(kBarQEmpty), 1);
+    mbar_init(bar(kBarQEmpty), 2);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bar(kBarFull + s), 1);
-      mbar_init(bar(kBarEmpty + s), 1);
+      mbar_init(bar(kBarEmpty + s), 2);  // released by both issuers
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(kBarSFull + t), 1);
       mbar_init(bar(kBarPFull + t), 4);  // one arrival per softmax warp
       mbar_init(bar(kBarOFull + t), 1);
     }
-    mbar_init(bar(kBarMmaDone), 1);
+    mbar_init(bar(kBarMmaDone), 2);
     // A timeout recorded by any earlier CTA or launch (and not yet cleared by
     // the host) makes this CTA skip its work: its rows come out as O = 0,
     // lse = -inf, and the host learns of it from the device error query.
     *abort_flag = *reinterpret_cast<volatile int *>(err) != kErrNone;
+    *turn = 0;
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -252,99 +259,121 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_drain(bar(kBarFull + i % C::kStages), (i / C::kStages) & 1, err);
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == kMmaWarp || warp == kMmaWarp1) {
+    // ------------------------------------------------------------ MMA issuers
+    // One issuing thread per query tile t, so that one tile's barrier waits
+    // and commits overlap the other tile's MMAs. Both consume every K/V ring
+    // slot of an item (each releases it once: the empty barriers count two
+    // arrivals); a tile that does not use a slot's tile waits for it to land
+    // before releasing it, so that its release always counts toward the
+    // phase the slot is in.
+    const int t = (warp == kMmaWarp) ? 0 : 1;
     if (lane == 0 && !skip) {
       constexpr uint32_t idesc_s = kFp8 ? idesc_e4m3_f32(128, 128) : idesc_bf16_f32(128, 128, false);
       constexpr uint32_t idesc_o = kFp8 ? idesc_e4m3_f32(128, D) : idesc_bf16_f32(128, D, true);
       constexpr int kKSteps = D * C::kElemBytes / 32;  // 32-byte K steps of S = Q K^T
-      const uint32_t q_base = smem_addr(sQ);
+      const uint32_t qt = smem_addr(sQ) + t * C::kTileBytes;
       const uint32_t ring_base = smem_addr(sRing);
+      const uint32_t s_col = tS(t), o_col = tO(t);
       int c = 0;             // ring position of the item's K_0
       int nq = 0;            // Q tile pairs consumed
-      int g[2] = {0, 0};     // KV steps done by each query tile over earlier items
+      int g = 0;             // KV steps done by this tile over earlier items
       bool ok = true;
+      int base = 0;          // burst slots of earlier items
       for (long long i = 0, k = item_index(0); k < n_items && ok; k = item_index(++i)) {
         const Item it = item_of(p, tbl, k);
-        const int n_t[2] = {tiles(it, 0), tiles(it, 1)};
-        const int n_max = max(n_t[0], n_t[1]);
+        const int nt = tiles(it, t);
+        const int n_max = max(tiles(it, 0), tiles(it, 1));
         if (n_max == 0) continue;
         if (!mbar_wait(bar(kBarQFull), nq & 1, abort_flag, err)) break;
         ++nq;
-        // Per KV step j: PV_0(j-1), S_0(j), PV_1(j-1), S_1(j). Both ring slots
-        // of the step are waited for first; each slot is released by a commit
-        // that fires when its last MMA completes.
+        if (nt == 0) mma_commit(bar(kBarQEmpty));  // this tile reads nothing of Q
+        // Burst slots alternate between the tiles: (step j, tile t) is slot
+        // base + 2 j + t. A tile waits for its data before its slot comes up
+        // and makes its commits after handing the slot on, so that its
+        // waits and commits overlap the other tile's MMAs.
         for (int j = 0; ok && j <= n_max; ++j) {
           const int cK = c + 2 * j, cV = c + 2 * j - 1;  // ring positions of K_j and V_{j-1}
           const int sK = cK % C::kStages, sV = (cV + C::kStages) % C::kStages;
+          const int cV2 = cK + 1, sV2 = cV2 % C::kStages;  // V_j
           const uint32_t k_base = ring_base + sK * C::kTileBytes;
           const uint32_t v_base = ring_base + sV * C::kTileBytes;
-          if (j < n_max && !mbar_wait(bar(kBarFull + sK), (cK / C::kStages) & 1, abort_flag, err)) {
+          const bool has_pv = j >= 1 && j - 1 < nt, has_s = j < nt, unused = !has_s && j < n_max;
+          // the data first (usually there already), the softmax's P last
+          if ((has_s || unused) && !mbar_wait(bar(kBarFull + sK), (cK / C::kStages) & 1, abort_flag, err)) {
             ok = false;
             break;
           }
-          if (j >= 1 && !mbar_wait(bar(kBarFull + sV), (cV / C::kStages) & 1, abort_flag, err)) {
+          if (unused && !mbar_wait(bar(kBarFull + sV2), (cV2 / C::kStages) & 1, abort_flag, err)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          for (int t = 0; t < 2 && ok; ++t) {
-            const int nt = n_t[t];
-            if (j >= 1 && j - 1 < nt) {
-              // O_t += P_t V_{j-1}; P_t was written over S_t by the softmax
-              // warps. For j = 1 this overwrites O_t: the warpgroup read the
-              // previous item's O_t before it signalled this P.
-              if (!mbar_wait(bar(kBarPFull + t), (g[t] + j - 1) & 1, abort_flag, err)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              if constexpr (kFp8) {
-                // B = V^T tile, K-major: 32 keys (32 bytes) per step; A = 8 TMEM columns of P
+          if (has_pv && (!mbar_wait(bar(kBarFull + sV), (cV / C::kStages) & 1, abort_flag, err) ||
+                         !mbar_wait(bar(kBarPFull + t), (g + j - 1) & 1, abort_flag, err))) {
+            ok = false;
+            break;
+          }
+          const int slot = base + 2 * j + t;
+          if (!wait_turn(turn, slot, abort_flag, err)) {
+            ok = false;
+            break;
+          }
+          if (has_pv) {
+            // O_t += P_t V_{j-1}; P_t was written over S_t by the softmax
+            // warps. For j = 1 this overwrites O_t: the warpgroup read the
+            // previous item's O_t before it signalled this P.
+            tc_fence_after();
+            if constexpr (kFp8) {
 #pragma unroll
-                for (int kk = 0; kk < kRowsPerTile / 32; ++kk)
-                  mma_ts_e4m3(tO(t), tS(t) + kk * 8, sw128_desc(v_base + kk * 32, 16, 1024), idesc_o,
-                              (j > 1 || kk > 0) ? 1u : 0u);
-              } else {
+              for (int kk = 0; kk < kRowsPerTile / 32; ++kk)
+                mma_ts_e4m3(o_col, s_col + kk * 8, sw128_desc(v_base + kk * 32, 16, 1024), idesc_o,
+                            (j > 1 || kk > 0) ? 1u : 0u);
+            } else {
+              // descriptor start fields advance by 2048 / 16 per 16 keys
+              const uint64_t vd = sw128_desc(v_base, kColBlockBytes, 1024);
+              mma_ts(o_col, s_col, vd, idesc_o, j > 1 ? 1u : 0u);
 #pragma unroll
-                for (int kk = 0; kk < kRowsPerTile / 16; ++kk) {
-                  const uint64_t bdesc = sw128_desc(v_base + kk * 2048, kColBlockBytes, 1024);
-                  mma_ts(tO(t), tS(t) + kk * 8, bdesc, idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
-                }
-              }
-              if (j - 1 == nt - 1) mma_commit(bar(kBarOFull + t));
-              if (t == 1 || j - 1 >= n_t[1]) mma_commit(bar(kBarEmpty + sV));  // last use of V_{j-1}
-            }
-            if (j < nt) {
-              // S_t = Q_t K_j^T
-              const uint32_t qt = q_base + t * C::kTileBytes;
-#pragma unroll
-              for (int kk = 0; kk < kKSteps; ++kk) {
-                const uint32_t off = (kk / 4) * kColBlockBytes + (kk % 4) * 32;
-                if constexpr (kFp8)
-                  mma_ss_e4m3(tS(t), sw128_desc(qt + off, 16, 1024), sw128_desc(k_base + off, 16, 1024),
-                              idesc_s, kk > 0 ? 1u : 0u);
-                else
-                  mma_ss(tS(t), sw128_desc(qt + off, 16, 1024), sw128_desc(k_base + off, 16, 1024),
-                         idesc_s, kk > 0 ? 1u : 0u);
-              }
-              mma_commit(bar(kBarSFull + t));
-              if (t == 1 || j >= n_t[1]) mma_commit(bar(kBarEmpty + sK));  // last use of K_j
+              for (int kk = 1; kk < kRowsPerTile / 16; ++kk)
+                mma_ts(o_col, s_col + kk * 8, vd + static_cast<uint64_t>(kk * 128), idesc_o, 1u);
             }
           }
-          // every S MMA of the item is issued: the Q buffer is free once they complete
-          if (ok && j == n_max - 1) mma_commit(bar(kBarQEmpty));
+          if (has_s) {
+            // S_t = Q_t K_j^T
+            const uint64_t qd = sw128_desc(qt, 16, 1024), kd = sw128_desc(k_base, 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < kKSteps; ++kk) {
+              const uint64_t off = static_cast<uint64_t>(((kk / 4) * kColBlockBytes + (kk % 4) * 32) >> 4);
+              if constexpr (kFp8)
+                mma_ss_e4m3(s_col, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+              else
+                mma_ss(s_col, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+            }
+          }
+          *turn = slot + 1;
+          if (has_s) mma_commit(bar(kBarSFull + t));
+          if (has_pv) {
+            if (j - 1 == nt - 1) mma_commit(bar(kBarOFull + t));
+            mma_commit(bar(kBarEmpty + sV));  // this tile's last use of V_{j-1}
+          }
+          if (has_s) {
+            mma_commit(bar(kBarEmpty + sK));  // this tile's use of K_j
+            if (j == nt - 1) mma_commit(bar(kBarQEmpty));  // this tile's last read of Q
+          }
+          if (unused) {  // K_j and V_j are not visible to this tile
+            mma_commit(bar(kBarEmpty + sK));
+            mma_commit(bar(kBarEmpty + sV2));
+          }
         }
         c += 2 * n_max;
-        g[0] += n_t[0];
-        g[1] += n_t[1];
+        g += nt;
+        base += 2 * (n_max + 1);
       }
       // All MMAs issued here must be complete before TMEM is released.
       mma_commit(bar(kBarMmaDone));
       mbar_drain(bar(kBarMmaDone), 0, err);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ softmax + epilogue
     const int t = warp >> 2;                         // query tile of this warpgroup
     const int row_in_tile = (warp & 3) * 32 + lane;  // TMEM lane = tile row

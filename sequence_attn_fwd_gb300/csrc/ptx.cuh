@@ -78,6 +78,29 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Waits until the shared counter *turn reaches `target` (another thread of
+// the CTA advances it); bounded like mbar_wait.
+__device__ __forceinline__ bool wait_turn(volatile int *turn, int target, volatile int *abort_flag,
+                                          int *err_word) {
+  if (*turn >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (*turn >= target) return true;
+    if ((n & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (*reinterpret_cast<volatile int *>(err_word) != kErrNone) {
+        *abort_flag = 1;
+        return false;
+      }
+      if (global_timer_ns() - t0 > SEQATTN_WAIT_TIMEOUT_NS) {
+        *abort_flag = 1;
+        atomicExch(err_word, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
 // Bounded wait that only gives up on time: used to drain this CTA's own
 // copies and MMAs in flight before it releases shared and tensor memory,
 // whatever the abort state.

@@ -205,7 +205,6 @@ __device__ __forceinline__ bool softmax_row(const AttnParams &p, const BlockDesc
     const float c2 = p.scale_log2;
     float m = -INFINITY;  // running max of scale*log2(e)*s (the reference for P)
     float l = 0.f;        // running sum of P relative to m
-    float m_grow = -INFINITY;  // candidate new reference from the latest tile
     bool ok = true;
 
     for (int j = 0; j < n; ++j) {
@@ -238,28 +237,36 @@ __device__ __forceinline__ bool softmax_row(const AttnParams &p, const BlockDesc
         }
       };
       uint32_t pk[64];
+      uint32_t sr[128];
+      load_scores(sr);
       float rowsum;
-      {
-        uint32_t sr[128];
-        load_scores(sr);
-        const float *s = reinterpret_cast<const float *>(sr);
-        if (j == 0) {
-          // no reference yet: the tile maximum first, then the exponentials
-          m = row_max(s) * c2;
-          rowsum = exp_row<false, kFp8>(s, c2, (m == -INFINITY) ? 0.f : m, pk, nullptr);
-        } else {
-          // Exponentiate against the current reference while finding the tile
-          // maximum; only if some row's maximum grew by more than 2^8 (rare
-          // after the first tiles) is O rescaled and the pass redone.
-          float mx;
-          rowsum = exp_row<true, kFp8>(s, c2, (m == -INFINITY) ? 0.f : m, pk, &mx);
-          m_grow = fmaxf(m, mx * c2);
-        }
-      }
-      if (j > 0) {
-        const float m_new = m_grow;
-        const bool grow = (m_new - m) > kRescaleThreshold;  // false while both are -inf
-        if (__any_sync(0xffffffffu, grow)) {
+      if (j == 0) {
+        // no reference yet: the tile maximum first, then the exponentials
+        m = row_max(reinterpret_cast<const float *>(sr)) * c2;
+        rowsum = exp_row<false, kFp8>(reinterpret_cast<const float *>(sr), c2,
+                                      (m == -INFINITY) ? 0.f : m, pk, nullptr);
+      } else {
+        // Exponentiate against the current reference. A row sum of at most
+        // 2^8 bounds every P by 2^8 (the bf16 P and the fp32 sums stay in
+        // range); only otherwise (rare after the first tiles), or while the
+        // row has no reference yet, is the tile maximum found, O rescaled and
+        // the pass redone.
+        rowsum = exp_row<false, kFp8>(reinterpret_cast<const float *>(sr), c2,
+                                      (m == -INFINITY) ? 0.f : m, pk, nullptr);
+        const bool big = !(rowsum <= 256.f) || (m == -INFINITY && rowsum > 0.f);
+        if (__any_sync(0xffffffffu, big)) {
+          // the tile maximum, 32 columns at a time (few live registers)
+          float mx = -INFINITY;
+#pragma unroll 1
+          for (int cb = 0; cb < 4; ++cb) {
+            uint32_t x[32];
+            tmem_ld32(s_addr + 32 * cb, x);
+            tmem_ld_wait(x);
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (!(tail || diag) || 32 * cb + c <= last) mx = fmaxf(mx, __uint_as_float(x[c]));
+          }
+          const float m_new = fmaxf(m, mx * c2);
           const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m - m_new);
           m = m_new;
           l *= alpha;
@@ -276,7 +283,6 @@ __device__ __forceinline__ bool softmax_row(const AttnParams &p, const BlockDesc
             tmem_st32(o_addr + 32 * cb, orr);
           }
           tmem_st_wait();
-          uint32_t sr[128];
           load_scores(sr);
           rowsum = exp_row<false, kFp8>(reinterpret_cast<const float *>(sr), c2,
                                         (m == -INFINITY) ? 0.f : m, pk, nullptr);

@@ -14,7 +14,10 @@ namespace detail {
 constexpr int kRowsPerTile = 128;  // MMA M and KV tile length
 constexpr int kColBlockBytes = 128 * 128;  // 128 rows x 128 bytes (64 bf16) swizzle block
 constexpr float kLn2 = 0.693147180559945309f;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows > 2^8
+// A row's P is formed against a lazily updated reference; the reference moves
+// (and O is rescaled) only when the tile's P would sum to more than 2^8,
+// which keeps every P at or below 2^8.
+constexpr float kRescaleSum = 256.0f;
 
 // The whole of a single problem as one block.
 __host__ __device__ __forceinline__ BlockDesc whole_problem(const AttnParams &p) {
@@ -87,17 +90,25 @@ __device__ __forceinline__ uint64_t exp2_poly_x2(uint64_t x) {
 }
 
 // Of every 8 pairs of a row's exponentials, this many take exp2_poly_x2 and
-// the rest the MUFU ex2.
-#ifndef SEQATTN_POLY_EXP_PAIRS_PER_8
-#define SEQATTN_POLY_EXP_PAIRS_PER_8 2
+// the rest the MUFU ex2 (GB300's MUFU does 32 ex2 per clock per SM, so the
+// softmax is bound by instruction issue rather than by the MUFU): none for
+// bf16 output and for e4m3 inputs, where every polynomial adds issue slots;
+// two for the fp32 partials, whose kernel measured faster with them (short
+// key chunks, where the fp32 epilogue's registers compete with the row's).
+#ifndef SEQATTN_POLY_EXP_PAIRS_PER_8_F32OUT
+#define SEQATTN_POLY_EXP_PAIRS_PER_8_F32OUT 2
 #endif
-constexpr int kPolyExpPairsPer8 = SEQATTN_POLY_EXP_PAIRS_PER_8;
-// The e4m3 kernel measured fastest with every exponential on the MUFU (its
-// softmax is bound by instruction issue, which the polynomial adds to).
+#ifndef SEQATTN_POLY_EXP_PAIRS_PER_8_BF16OUT
+#define SEQATTN_POLY_EXP_PAIRS_PER_8_BF16OUT 0
+#endif
 #ifndef SEQATTN_POLY_EXP_PAIRS_PER_8_FP8
 #define SEQATTN_POLY_EXP_PAIRS_PER_8_FP8 0
 #endif
-constexpr int kPolyExpPairsPer8Fp8 = SEQATTN_POLY_EXP_PAIRS_PER_8_FP8;
+template <bool kF32Out, bool kFp8>
+constexpr int poly_pairs_per_8() {
+  return kFp8 ? SEQATTN_POLY_EXP_PAIRS_PER_8_FP8
+              : (kF32Out ? SEQATTN_POLY_EXP_PAIRS_PER_8_F32OUT : SEQATTN_POLY_EXP_PAIRS_PER_8_BF16OUT);
+}
 
 __device__ __forceinline__ uint64_t exp2_pair(uint64_t x, bool poly) {
   if (poly) return exp2_poly_x2(x);
@@ -108,28 +119,20 @@ __device__ __forceinline__ uint64_t exp2_pair(uint64_t x, bool poly) {
 
 // P = 2^(s * c2 - m_ref) for the 128 scores of a row, packed as bf16 pairs
 // (element 2i in the low half) or, with kFp8, as e4m3 quads, returning the
-// fp32 sum of the unrounded P. With kTrackMax the raw row maximum is found in
-// the same pass.
-template <bool kTrackMax, bool kFp8 = false>
-__device__ __forceinline__ float exp_row(const float *s, float c2, float m_ref, uint32_t *pk,
-                                         float *mx_out) {
+// fp32 sum of the unrounded P; kPoly of every 8 pairs take exp2_poly_x2.
+template <bool kFp8, int kPoly>
+__device__ __forceinline__ float exp_row(const float *s, float c2, float m_ref, uint32_t *pk) {
   const uint64_t scale2 = f2_pack(c2, c2);
   const uint64_t neg_m2 = f2_pack(-m_ref, -m_ref);
   uint64_t sum_a = f2_pack(0.f, 0.f), sum_b = sum_a;
-  float ma = -INFINITY, mb = -INFINITY;
 #pragma unroll
   for (int q = 0; q < 64; q += 2) {  // pairs q and q + 1: elements 2q .. 2q + 3
-    constexpr int kPoly = kFp8 ? kPolyExpPairsPer8Fp8 : kPolyExpPairsPer8;
     const uint64_t pa = exp2_pair(f2_fma(f2_pack(s[2 * q], s[2 * q + 1]), scale2, neg_m2),
                                   (q % 8) < kPoly);
     const uint64_t pb = exp2_pair(f2_fma(f2_pack(s[2 * q + 2], s[2 * q + 3]), scale2, neg_m2),
                                   ((q + 1) % 8) < kPoly);
     sum_a = f2_add(sum_a, pa);
     sum_b = f2_add(sum_b, pb);
-    if (kTrackMax) {
-      ma = fmax3(ma, s[2 * q], s[2 * q + 1]);
-      mb = fmax3(mb, s[2 * q + 2], s[2 * q + 3]);
-    }
     float p0, p1, p2, p3;
     f2_unpack(pa, p0, p1);
     f2_unpack(pb, p2, p3);
@@ -142,7 +145,6 @@ __device__ __forceinline__ float exp_row(const float *s, float c2, float m_ref, 
       pk[q + 1] = *reinterpret_cast<uint32_t *>(&h1);
     }
   }
-  if (kTrackMax) *mx_out = fmaxf(ma, mb);
   float a0, a1, b0, b1;
   f2_unpack(sum_a, a0, a1);
   f2_unpack(sum_b, b0, b1);
@@ -203,6 +205,7 @@ __device__ __forceinline__ bool softmax_row(const AttnParams &p, const BlockDesc
     const long long qpos = blk.q_pos + row;
     const long long tile_first_q = blk.q_pos + tile_first_row;
     const float c2 = p.scale_log2;
+    constexpr int kPoly = poly_pairs_per_8<kF32Out, kFp8>();
     float m = -INFINITY;  // running max of scale*log2(e)*s (the reference for P)
     float l = 0.f;        // running sum of P relative to m
     bool ok = true;
@@ -243,17 +246,17 @@ __device__ __forceinline__ bool softmax_row(const AttnParams &p, const BlockDesc
       if (j == 0) {
         // no reference yet: the tile maximum first, then the exponentials
         m = row_max(reinterpret_cast<const float *>(sr)) * c2;
-        rowsum = exp_row<false, kFp8>(reinterpret_cast<const float *>(sr), c2,
-                                      (m == -INFINITY) ? 0.f : m, pk, nullptr);
+        rowsum = exp_row<kFp8, kPoly>(reinterpret_cast<const float *>(sr), c2,
+                                      (m == -INFINITY) ? 0.f : m, pk);
       } else {
         // Exponentiate against the current reference. A row sum of at most
         // 2^8 bounds every P by 2^8 (the bf16 P and the fp32 sums stay in
         // range); only otherwise (rare after the first tiles), or while the
         // row has no reference yet, is the tile maximum found, O rescaled and
         // the pass redone.
-        rowsum = exp_row<false, kFp8>(reinterpret_cast<const float *>(sr), c2,
-                                      (m == -INFINITY) ? 0.f : m, pk, nullptr);
-        const bool big = !(rowsum <= 256.f) || (m == -INFINITY && rowsum > 0.f);
+        rowsum = exp_row<kFp8, kPoly>(reinterpret_cast<const float *>(sr), c2,
+                                      (m == -INFINITY) ? 0.f : m, pk);
+        const bool big = !(rowsum <= kRescaleSum) || (m == -INFINITY && rowsum > 0.f);
         if (__any_sync(0xffffffffu, big)) {
           // the tile maximum, 32 columns at a time (few live registers)
           float mx = -INFINITY;
@@ -284,8 +287,8 @@ __device__ __forceinline__ bool softmax_row(const AttnParams &p, const BlockDesc
           }
           tmem_st_wait();
           load_scores(sr);
-          rowsum = exp_row<false, kFp8>(reinterpret_cast<const float *>(sr), c2,
-                                        (m == -INFINITY) ? 0.f : m, pk, nullptr);
+          rowsum = exp_row<kFp8, kPoly>(reinterpret_cast<const float *>(sr), c2,
+                                        (m == -INFINITY) ? 0.f : m, pk);
         }
       }
       l += rowsum;

@@ -74,7 +74,7 @@ class Workload:
         return f * 0.5 if self.causal else f
 
 
-# The six workloads the attention path is checked and measured on.
+# The workloads the attention path is checked and measured on.
 WORKLOADS = {
     w.name: w
     for w in [
@@ -87,6 +87,13 @@ WORKLOADS = {
                  sample_rows=64),
         Workload("varlen_hq32hkv8t65536d128_causal", 1, 32, 8, 65536, 128, True, 1, 1006,
                  varlen=True),
+        # Reduced forms of the 131K ring for profiling under ncu (a few GB on the
+        # device): the same heads and key-chunk length (8192) over a quarter of
+        # the sequence, and the same 16-way merge over a quarter of the rows.
+        Workload("ring4_b1hq32hkv8s32768d128_causal", 1, 32, 8, 32768, 128, True, 4, 1007,
+                 sample_rows=64),
+        Workload("ring16_b1hq32hkv8s32768d128_causal", 1, 32, 8, 32768, 128, True, 16, 1008,
+                 sample_rows=64),
     ]
 }
 

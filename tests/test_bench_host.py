@@ -91,7 +91,13 @@ def test_workload_sizes_match_the_stated_configurations():
     W = workloads.WORKLOADS
     assert [(w.B, w.Hq, w.Hkv, w.S, w.D, w.causal, w.P) for w in W.values()] == [
         (1, 2, 2, 256, 64, False, 1), (2, 32, 32, 4096, 128, True, 8), (1, 28, 4, 32768, 128, True, 1),
-        (2, 32, 32, 8192, 128, True, 16), (1, 32, 8, 131072, 128, True, 16), (1, 32, 8, 65536, 128, True, 1)]
+        (2, 32, 32, 8192, 128, True, 16), (1, 32, 8, 131072, 128, True, 16), (1, 32, 8, 65536, 128, True, 1),
+        (1, 32, 8, 32768, 128, True, 4), (1, 32, 8, 32768, 128, True, 16)]
+    # the reduced forms of the 131K ring keep its heads and, respectively, its
+    # key-chunk length and its part count
+    big = W["ring16_b1hq32hkv8s131072d128_causal"]
+    assert W["ring4_b1hq32hkv8s32768d128_causal"].chunk == big.chunk
+    assert W["ring16_b1hq32hkv8s32768d128_causal"].P == big.P
     v = W["varlen_hq32hkv8t65536d128_causal"]
     lens = workloads.seq_lens(v)
     assert lens.sum() == v.S and lens.min() >= 1 and lens[:-1].min() >= 128 and lens.max() <= 8192

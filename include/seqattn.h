@@ -231,11 +231,11 @@ int attn_fwd_fp8(const void *q8, const void *k8, const void *vt8, void *o, float
  *   P = exp(scale Q K^T - lse),  delta_i = <dO_i, O_i>,
  *   dV = P^T dO,  dS = P * (dO V^T - delta),  dK = scale dS^T Q,  dQ = scale dS K,
  * dK and dV summed over the query heads of each GQA group.
- *   q, o, dout  bf16 [B, Hq, S, 128];  k, v  bf16 [B, Hkv, S, 128]
+ *   q, o, dout  bf16 [B, Hq, S, D];  k, v  bf16 [B, Hkv, S, D]
  *   lse         fp32 [B, Hq, S] from attn_fwd (natural log)
  *   delta       fp32 [B, Hq, S] workspace (written, then read)
- *   dq          bf16 [B, Hq, S, 128];  dk, dv  bf16 [B, Hkv, S, 128]  (outputs)
- * Head dim 128 only and S <= 65535 * 128 (else ATTN_ERR_UNSUPPORTED); bad
+ *   dq          bf16 [B, Hq, S, D];  dk, dv  bf16 [B, Hkv, S, D]  (outputs)
+ * D in {64, 128} and S <= 65535 * 128 (else ATTN_ERR_UNSUPPORTED); bad
  * shapes, scale, pointers or alignment: ATTN_ERR_INVALID_ARG. Device pointers
  * owned by the caller; asynchronous on `stream`.
  */

@@ -225,8 +225,9 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
              dq: torch.Tensor | None = None, dk: torch.Tensor | None = None, dv: torch.Tensor | None = None,
              delta: torch.Tensor | None = None):
     """Gradients (dQ, dK, dV) of attn_fwd(q, k, v) for the output gradient dout,
-    from the forward's o and lse (bf16 [B,Hq,S,128] q / o / dout, [B,Hkv,S,128]
-    k / v, fp32 lse [B,Hq,S]). delta is an optional fp32 [B,Hq,S] workspace."""
+    from the forward's o and lse (bf16 [B,Hq,S,D] q / o / dout, [B,Hkv,S,D]
+    k / v with D 64 or 128, fp32 lse [B,Hq,S]). delta is an optional fp32
+    [B,Hq,S] workspace."""
     _require(q.dim() == 4 and k.dim() == 4 and v.shape == k.shape, "expected [B,H,S,D] tensors")
     B, Hq, S, D = q.shape
     Hkv = k.shape[1]

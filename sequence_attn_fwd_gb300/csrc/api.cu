@@ -244,7 +244,7 @@ int attn_bwd(const void *q, const void *k, const void *v, const void *o, const f
   if (B < 0 || Hq <= 0 || Hkv <= 0 || S < 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
   if (!scale_ok(scale)) return ATTN_ERR_INVALID_ARG;
-  if (D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
   if (S > 65535ll * 128) return ATTN_ERR_UNSUPPORTED;  // 128-row tiles along the grid's y
   if (static_cast<long long>(B) * Hq > 0x7fffffffll) return ATTN_ERR_UNSUPPORTED;
   if (B == 0 || S == 0) return ATTN_OK;
@@ -271,7 +271,7 @@ int attn_bwd(const void *q, const void *k, const void *v, const void *o, const f
   p.S = S;
   p.scale = scale;
   p.causal = causal;
-  cudaError_t e = seqattn::launch_attention_bwd(tq, tk, tv, tdo, o, dout, delta, p,
+  cudaError_t e = seqattn::launch_attention_bwd(D, tq, tk, tv, tdo, o, dout, delta, p,
                                                 reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }

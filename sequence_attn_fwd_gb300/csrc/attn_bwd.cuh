@@ -1,4 +1,4 @@
-// Backward of blockwise attention for sm_103a (head dim 128, bf16): the
+// Backward of blockwise attention for sm_103a (head dim 64 or 128, bf16): the
 // gradients dQ, dK, dV for an output gradient dO, recomputing the scores
 // tile by tile from Q, K and the forward's lse instead of storing the [S, S]
 // probabilities (the backward the page "ms-swift集成FlashAttention 2/3，长文本
@@ -34,34 +34,41 @@
 namespace seqattn {
 namespace bwd {
 
-constexpr int kD = 128;
 constexpr int kRows = 128;                      // tile rows (keys or queries)
-constexpr int kTileBytes = kRows * kD * 2;      // 32 KB: two 128-byte column blocks
-constexpr int kColBlock = kRows * 128;          // 16 KB
-constexpr int kStages = 4;                      // ring slots of 32 KB
+constexpr int kColBlock = kRows * 128;          // 16 KB: 128 rows of one 128-byte column block
 constexpr int kThreads = 576;
 constexpr int kMmaWarp = 16, kTmaWarp = 17;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// barriers: stay_full, full[S], empty[S / 2] (one per iteration's pair of
-// slots), st_full[2], pt_full[2], acc_done
-constexpr int kNumBarriers = 1 + kStages + kStages / 2 + 5;
-constexpr int kSmemBytes = 1024 + 2 * kTileBytes + kStages * kTileBytes + 2 * 2 * kRows * 4 +
-                           8 * kNumBarriers + 16;
+// Shared-memory plan for head dim D: tiles of 128 rows x D bf16 (D / 64
+// column blocks), a 128 KB ring of them.
+template <int D>
+struct BwdCfg {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kTileBytes = kRows * D * 2;
+  static constexpr int kStages = 131072 / kTileBytes;  // 4 slots of 32 KB or 8 of 16 KB
+  // barriers: stay_full, full[S], empty[S / 2] (one per iteration's pair of
+  // slots), st_full[2], pt_full[2], acc_done
+  static constexpr int kNumBarriers = 1 + kStages + kStages / 2 + 5;
+  static constexpr int kSmemBytes = 1024 + 2 * kTileBytes + kStages * kTileBytes + 2 * 2 * kRows * 4 +
+                                    8 * kNumBarriers + 16;
+};
 
-// Loads a 128 x 128 bf16 tile (two 64-column boxes) into `dst`.
+// Loads a 128 x D bf16 tile (one 64-column box per column block) into `dst`.
+template <int D>
 __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap *map, uint32_t bar, int row,
                                           int head) {
-  tma_load_3d(dst, map, bar, 0, row, head);
-  tma_load_3d(dst + kColBlock, map, bar, 64, row, head);
+#pragma unroll
+  for (int cb = 0; cb < D / 64; ++cb) tma_load_3d(dst + cb * kColBlock, map, bar, 64 * cb, row, head);
 }
 
-// One 64-column half of S (or S^T) = A B^T over D = 128: A a 128-row K-major
+// One 64-column half of S (or S^T) = A B^T over D: A a 128-row K-major
 // tile, B the 64 rows of a K-major tile starting at `b` (a multiple of 8 rows).
+template <int D>
 __device__ __forceinline__ void mma_rows_dot(uint32_t d_tmem, uint32_t a, uint32_t b) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 64, false);
 #pragma unroll
-  for (int kk = 0; kk < kD / 16; ++kk) {
+  for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = (kk / 4) * kColBlock + (kk % 4) * 32;
     mma_ss(d_tmem, sw128_desc(a + off, 16, 1024), sw128_desc(b + off, 16, 1024), idesc,
            kk > 0 ? 1u : 0u);
@@ -69,14 +76,15 @@ __device__ __forceinline__ void mma_rows_dot(uint32_t d_tmem, uint32_t a, uint32
 }
 
 // acc (+)= A_h B_h for contraction half h: A = 128 x 128 bf16 in TMEM
-// (contraction over its columns), B = 128 x 128 tile in shared memory whose
+// (contraction over its columns), B = 128 x D tile in shared memory whose
 // rows are the contraction index (N-contiguous operand); half h covers
 // contraction elements [64h, 64h + 64). A's elements are packed as bf16 pairs:
 // the element-wise warpgroup of columns [32c, 32c + 32) packs them over the
 // first 16 of its own TMEM columns, so elements 16k..16k+15 sit in the 8
 // columns at a_tmem + 32(k/2) + 8(k%2).
+template <int D>
 __device__ __forceinline__ void mma_acc_tmem(uint32_t acc, uint32_t a_tmem, uint32_t b, int h, bool first) {
-  constexpr uint32_t idesc = idesc_bf16_f32(128, kD, true);
+  constexpr uint32_t idesc = idesc_bf16_f32(128, D, true);
 #pragma unroll
   for (int k4 = 0; k4 < 4; ++k4) {
     const int kk = 4 * h + k4;
@@ -90,22 +98,23 @@ __device__ __forceinline__ void mma_acc_tmem(uint32_t acc, uint32_t a_tmem, uint
 // loads (they are warp-wide); only lanes with `valid` store.
 template <int NC>
 __device__ __forceinline__ void store_acc_row(uint32_t taddr, float mul, __nv_bfloat16 *dst, bool valid) {
+  static_assert(NC % 16 == 0, "16-column chunks");
 #pragma unroll 1
-  for (int cb = 0; cb < NC / 32; ++cb) {
-    uint32_t r[32];
-    tmem_ld32(taddr + 32 * cb, r);
+  for (int cb = 0; cb < NC / 16; ++cb) {
+    uint32_t r[16];
+    tmem_ld16(taddr + 16 * cb, r);
     tmem_ld_wait(r);
-    uint32_t pk[16];
+    uint32_t pk[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 8; ++i) {
       __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[2 * i]) * mul,
                                                __uint_as_float(r[2 * i + 1]) * mul);
       pk[i] = *reinterpret_cast<uint32_t *>(&h);
     }
     if (valid) {
-      uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * cb);
+      uint4 *d4 = reinterpret_cast<uint4 *>(dst + 16 * cb);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      for (int i = 0; i < 2; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
     }
   }
 }
@@ -116,19 +125,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // ---------------------------------------------------------------- delta
+// A warp per row; lane l reads elements [D/32 l, D/32 (l + 1)) of O and dO.
+template <int D>
 __global__ void delta_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dout,
                              float *__restrict__ delta, long long nrows) {
+  using Vec = typename std::conditional<D == 128, uint2, uint32_t>::type;  // D / 32 bf16 per lane
   const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
   const int lane = threadIdx.x & 31;
   for (long long r = warp; r < nrows; r += nwarps) {
-    const uint2 a = reinterpret_cast<const uint2 *>(o + r * kD)[lane];
-    const uint2 b = reinterpret_cast<const uint2 *>(dout + r * kD)[lane];
+    const Vec a = reinterpret_cast<const Vec *>(o + r * D)[lane];
+    const Vec b = reinterpret_cast<const Vec *>(dout + r * D)[lane];
     const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a);
     const __nv_bfloat162 *pb = reinterpret_cast<const __nv_bfloat162 *>(&b);
     float s = 0.f;
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < D / 64; ++i) {
       const float2 fa = __bfloat1622float2(pa[i]), fb = __bfloat1622float2(pb[i]);
       s = fmaf(fa.x, fb.x, s);
       s = fmaf(fa.y, fb.y, s);
@@ -143,11 +155,13 @@ __global__ void delta_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfl
 // kDq = false: the dK / dV kernel (grid: key tiles x B*Hkv); kDq = true: the
 // dQ kernel (grid: query tiles x B*Hq). "Stay" tiles are loaded once (K, V or
 // Q, dO); "stream" tiles pass through the ring (Q_i, dO_i or K_j, V_j).
-template <bool kDq>
+template <int D, bool kDq>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const BwdParams p) {
+  using C = BwdCfg<D>;
+  constexpr int kTileBytes = C::kTileBytes, kStages = C::kStages, kNumBarriers = C::kNumBarriers;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -209,8 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const bool skip = *abort_flag != 0;
   // TMEM: S or S^T [0,128) (then P / dS as bf16 pairs in columns [0,32) and [64,96)),
-  // dP or dP^T [128,256), accumulators [256,384) and (dK/dV) [384,512)
-  const uint32_t tS = tmem, tDP = tmem + 128, tAcc0 = tmem + 256, tAcc1 = tmem + 384;
+  // dP or dP^T [128,256), accumulators [256,256+D) and (dK/dV) [256+D,256+2D)
+  const uint32_t tS = tmem, tDP = tmem + 128, tAcc0 = tmem + 256, tAcc1 = tmem + 256 + D;
 
   if (warp == kTmaWarp) {
     if (lane == 0 && !skip && n_iter > 0) {
@@ -220,11 +234,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&tm_do);
       mbar_arrive_expect_tx(bar(kBarStay), 2 * kTileBytes);
       if (kDq) {
-        load_tile(smem_addr(sStay), &tm_q, bar(kBarStay), tile * kRows, head);
-        load_tile(smem_addr(sStay + kTileBytes), &tm_do, bar(kBarStay), tile * kRows, head);
+        load_tile<D>(smem_addr(sStay), &tm_q, bar(kBarStay), tile * kRows, head);
+        load_tile<D>(smem_addr(sStay + kTileBytes), &tm_do, bar(kBarStay), tile * kRows, head);
       } else {
-        load_tile(smem_addr(sStay), &tm_k, bar(kBarStay), tile * kRows, head);
-        load_tile(smem_addr(sStay + kTileBytes), &tm_v, bar(kBarStay), tile * kRows, head);
+        load_tile<D>(smem_addr(sStay), &tm_k, bar(kBarStay), tile * kRows, head);
+        load_tile<D>(smem_addr(sStay + kTileBytes), &tm_v, bar(kBarStay), tile * kRows, head);
       }
       const int kv_head = kDq ? b * p.Hkv + (head % p.Hq) / group : head;
       int c = 0;
@@ -239,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int slot = c % kStages;
           mbar_arrive_expect_tx(bar(kBarFull + slot), kTileBytes);
           const CUtensorMap *map = kDq ? (which ? &tm_v : &tm_k) : (which ? &tm_do : &tm_q);
-          load_tile(smem_addr(sRing + slot * kTileBytes), map, bar(kBarFull + slot), row,
+          load_tile<D>(smem_addr(sRing + slot * kTileBytes), map, bar(kBarFull + slot), row,
                     kDq ? kv_head : q_head);
         }
       }
@@ -265,16 +279,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto ring0 = [&](int it) { return ring + ((2 * it) % kStages) * kTileBytes; };
       auto ring1 = [&](int it) { return ring + ((2 * it + 1) % kStages) * kTileBytes; };
       auto scores = [&](int it, int h) {  // S = Q K_j^T, dP = dO V_j^T (or S^T = K Q_i^T, dP^T = V dO_i^T)
-        mma_rows_dot(tS + 64 * h, stay0, ring0(it) + 8192 * h);
-        mma_rows_dot(tDP + 64 * h, stay1, ring1(it) + 8192 * h);
+        mma_rows_dot<D>(tS + 64 * h, stay0, ring0(it) + 8192 * h);
+        mma_rows_dot<D>(tDP + 64 * h, stay1, ring1(it) + 8192 * h);
         mma_commit(bar(kBarSt + h));
       };
       auto accumulate = [&](int it, int h) {
         if (kDq) {
-          mma_acc_tmem(tAcc0, tS, ring0(it), h, it == 0 && h == 0);   // dQ += dS K_j
+          mma_acc_tmem<D>(tAcc0, tS, ring0(it), h, it == 0 && h == 0);   // dQ += dS K_j
         } else {
-          mma_acc_tmem(tAcc0, tS, ring1(it), h, it == 0 && h == 0);   // dV += P^T dO_i
-          mma_acc_tmem(tAcc1, tDP, ring0(it), h, it == 0 && h == 0);  // dK += dS^T Q_i
+          mma_acc_tmem<D>(tAcc0, tS, ring1(it), h, it == 0 && h == 0);   // dV += P^T dO_i
+          mma_acc_tmem<D>(tAcc1, tDP, ring0(it), h, it == 0 && h == 0);  // dK += dS^T Q_i
         }
       };
       // The issuing thread's waits, commits and fences stall the tensor pipe
@@ -420,16 +434,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warp-uniform branches only around the TMEM loads; the row bound guards the stores
     const bool valid = my_row < S;
     const size_t row_off = static_cast<size_t>(head) * S + (valid ? my_row : 0);
-    if (kDq) {  // dQ = scale dS K: warpgroup w stores columns [32w, 32w + 32)
-      __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.dq) + row_off * kD + 32 * wg;
-      if (done) store_acc_row<32>(tAcc0 + lane_off + 32 * wg, p.scale, dst, valid);
-      else if (valid) for (int d = 0; d < 32; ++d) dst[d] = __float2bfloat16(0.f);
-    } else {  // warpgroups 0, 1: dV columns [0, 64), [64, 128); 2, 3: dK (times scale)
+    if (kDq) {  // dQ = scale dS K: warpgroup w stores columns [D/4 w, D/4 (w + 1))
+      constexpr int kNc = D / 4;
+      __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.dq) + row_off * D + kNc * wg;
+      if (done) store_acc_row<kNc>(tAcc0 + lane_off + kNc * wg, p.scale, dst, valid);
+      else if (valid) for (int d = 0; d < kNc; ++d) dst[d] = __float2bfloat16(0.f);
+    } else {  // warpgroups 0, 1: dV columns [0, D/2), [D/2, D); 2, 3: dK (times scale)
+      constexpr int kNc = D / 2;
       const bool is_dk = wg >= 2;
-      const int cofs = 64 * (wg & 1);
-      __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(is_dk ? p.dk : p.dv) + row_off * kD + cofs;
-      if (done) store_acc_row<64>((is_dk ? tAcc1 : tAcc0) + lane_off + cofs, is_dk ? p.scale : 1.f, dst, valid);
-      else if (valid) for (int d = 0; d < 64; ++d) dst[d] = __float2bfloat16(0.f);
+      const int cofs = kNc * (wg & 1);
+      __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(is_dk ? p.dk : p.dv) + row_off * D + cofs;
+      if (done) store_acc_row<kNc>((is_dk ? tAcc1 : tAcc0) + lane_off + cofs, is_dk ? p.scale : 1.f, dst, valid);
+      else if (valid) for (int d = 0; d < kNc; ++d) dst[d] = __float2bfloat16(0.f);
     }
   }
 

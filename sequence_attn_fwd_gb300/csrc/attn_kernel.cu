@@ -491,29 +491,42 @@ cudaError_t launch_attention_blocks(int D, bool f32_out, const CUtensorMap &tq,
   return launch_dispatch(D, f32_out, tq, tk, tv, to, p, tbl, tbl.item_start[tbl.n], stream);
 }
 
-cudaError_t launch_attention_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                                 const CUtensorMap &tdo, const void *o, const void *dout,
-                                 float *delta, const BwdParams &p, cudaStream_t stream) {
+namespace {
+
+template <int D>
+cudaError_t launch_bwd_typed(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                             const CUtensorMap &tdo, const void *o, const void *dout, float *delta,
+                             const BwdParams &p, cudaStream_t stream) {
   const long long nrows = static_cast<long long>(p.B) * p.Hq * p.S;
   if (nrows == 0) return cudaSuccess;
   long long blocks = (nrows + 7) / 8;  // 8 warps of 256 threads, a row per warp
   const long long cap = static_cast<long long>(sm_count()) * 8;
   if (blocks > cap) blocks = cap;
-  bwd::delta_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+  bwd::delta_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16 *>(o), static_cast<const __nv_bfloat16 *>(dout), delta, nrows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const unsigned n_tiles = static_cast<unsigned>((p.S + bwd::kRows - 1) / bwd::kRows);
+  constexpr int kSmem = bwd::BwdCfg<D>::kSmemBytes;
   for (int dq = 0; dq < 2; ++dq) {
-    auto kernel = dq ? bwd::attn_bwd_kernel<true> : bwd::attn_bwd_kernel<false>;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bwd::kSmemBytes);
+    auto kernel = dq ? bwd::attn_bwd_kernel<D, true> : bwd::attn_bwd_kernel<D, false>;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>(p.B * (dq ? p.Hq : p.Hkv)), n_tiles);
-    kernel<<<grid, bwd::kThreads, bwd::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+    kernel<<<grid, bwd::kThreads, kSmem, stream>>>(tq, tk, tv, tdo, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_attention_bwd(int D, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                                 const CUtensorMap &tdo, const void *o, const void *dout,
+                                 float *delta, const BwdParams &p, cudaStream_t stream) {
+  return D == 64 ? launch_bwd_typed<64>(tq, tk, tv, tdo, o, dout, delta, p, stream)
+                 : launch_bwd_typed<128>(tq, tk, tv, tdo, o, dout, delta, p, stream);
 }
 
 // A one-CTA kernel waiting on an mbarrier that nothing ever arrives at, with

@@ -51,7 +51,7 @@ cudaError_t launch_attention(int D, bool f32_out, const CUtensorMap &tm_q, const
                              const CUtensorMap &tm_v, const CUtensorMap &tm_o, const AttnParams &p,
                              cudaStream_t stream);
 
-// Backward (head dim 128): gradients of a forward whose O and lse are given.
+// Backward (head dim 64 or 128): gradients of a forward whose O and lse are given.
 struct BwdParams {
   const float *lse;    // [B*Hq, S] natural log (the forward's)
   const float *delta;  // [B*Hq, S] workspace: <dO_i, O_i>, written by the first kernel
@@ -62,8 +62,8 @@ struct BwdParams {
 };
 
 // delta, then dK / dV (grid: key tiles x B*Hkv), then dQ (grid: query tiles x
-// B*Hq); maps over bf16 [heads][S][128], box 64 x 128 x 1, 128-byte swizzle.
-cudaError_t launch_attention_bwd(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+// B*Hq); maps over bf16 [heads][S][D], box 64 x 128 x 1, 128-byte swizzle.
+cudaError_t launch_attention_bwd(int D, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                  const CUtensorMap &tm_v, const CUtensorMap &tm_do,
                                  const void *o, const void *dout, float *delta,
                                  const BwdParams &p, cudaStream_t stream);

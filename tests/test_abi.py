@@ -178,7 +178,8 @@ def test_attn_bwd_argument_checks(lib):
         return lib.attn_bwd(q, FAKE, FAKE, FAKE, FAKE, FAKE, delta, FAKE, FAKE, FAKE, B, Hq, Hkv, S, D, 1,
                             ctypes.c_float(scale), None)
 
-    assert run(D=64) == 2
+    assert run(D=96) == 2 and run(D=32) == 2
+    assert run(D=64, q=FAKE + 8) == 1  # D = 64 is accepted: it reaches the alignment checks
     assert run(S=65536 * 128) == 2  # more than 65535 tiles of 128 rows
     assert run(Hq=3, Hkv=2) == 1 and run(scale=-1.0) == 1
     assert run(q=FAKE + 8) == 1 and run(delta=FAKE + 2) == 1 and run(q=0) == 1

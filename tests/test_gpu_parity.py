@@ -339,14 +339,14 @@ def test_attn_fwd_fp8_against_oracle(sa, shape):
     assert head_dev <= FP8_SLOPE_TOL and col_dev <= FP8_SLOPE_TOL, (head_dev, col_dev)
 
 
-@pytest.mark.parametrize("shape", [(1, 2, 2, 256, True), (1, 4, 2, 300, True), (2, 2, 1, 200, False)],
-                         ids=["s256c", "gqa_s300c", "b2_s200"])
+@pytest.mark.parametrize("shape", [(1, 2, 2, 256, True, 128), (1, 4, 2, 300, True, 128), (2, 2, 1, 200, False, 128),
+                                   (1, 2, 2, 256, True, 64), (1, 4, 2, 300, True, 64), (2, 2, 1, 200, False, 64)],
+                         ids=["s256c", "gqa_s300c", "b2_s200", "d64_s256c", "d64_gqa_s300c", "d64_b2_s200"])
 def test_attn_bwd_against_oracle(sa, shape):
     """dQ, dK, dV (from the oracle's O and lse as the backward's inputs) against
     the oracle's exact gradients, each element within the bound derived in
-    bwd_bound."""
-    B, Hq, Hkv, S, causal = shape
-    D = 128
+    bwd_bound; head dims 128 and 64."""
+    B, Hq, Hkv, S, causal, D = shape
     q, k, v = workloads.make_qkv(adhoc(B, Hq, Hkv, S, D, causal, seed=71))
     dout, _, _ = workloads.make_qkv(adhoc(B, Hq, Hq, S, D, causal, seed=72))
     qd, kd, vd, dod = to_dev(q, k, v, dout)

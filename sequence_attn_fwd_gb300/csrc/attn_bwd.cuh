@@ -62,11 +62,11 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap *map, 
   for (int cb = 0; cb < D / 64; ++cb) tma_load_3d(dst + cb * kColBlock, map, bar, 64 * cb, row, head);
 }
 
-// One 64-column half of S (or S^T) = A B^T over D: A a 128-row K-major
-// tile, B the 64 rows of a K-major tile starting at `b` (a multiple of 8 rows).
+// S (or S^T) = A B^T over D: A and B 128-row K-major tiles (N = 128: the
+// full-rate shape; N = 64 halves are bound by shared-memory reads).
 template <int D>
 __device__ __forceinline__ void mma_rows_dot(uint32_t d_tmem, uint32_t a, uint32_t b) {
-  constexpr uint32_t idesc = idesc_bf16_f32(128, 64, false);
+  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = (kk / 4) * kColBlock + (kk % 4) * 32;
@@ -205,10 +205,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarStay), 1);
     for (int s = 0; s < kStages; ++s) mbar_init(bar(kBarFull + s), 1);
     for (int s = 0; s < kStages / 2; ++s) mbar_init(bar(kBarEmpty + s), 1);
-    for (int h = 0; h < 2; ++h) {
-      mbar_init(bar(kBarSt + h), 1);
-      mbar_init(bar(kBarPt + h), 8);  // one arrival per warp of the two warpgroups of half h
-    }
+    mbar_init(bar(kBarSt), 1);      // S (or S^T) computed
+    mbar_init(bar(kBarSt + 1), 1);  // dP (or dP^T) computed
+    mbar_init(bar(kBarPt), 16);     // P^T in TMEM (dK/dV): one arrival per element-wise warp
+    mbar_init(bar(kBarPt + 1), 16); // dS (or dS^T) in TMEM
     mbar_init(bar(kBarAcc), 1);
     *abort_flag = *reinterpret_cast<volatile int *>(err) != kErrNone;
     fence_barrier_init();
@@ -266,11 +266,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && !skip && n_iter > 0) {
       const uint32_t stay0 = smem_addr(sStay), stay1 = stay0 + kTileBytes;
       const uint32_t ring = smem_addr(sRing);
-      // Half h of iteration it: S / dP columns [64h, 64h + 64) (element-wise
-      // warpgroup h), then the accumulations over that half. Each half's
-      // accumulation is issued once its warpgroup is done, followed by the
-      // next iteration's scores of the same half, so one warpgroup's
-      // element-wise pass overlaps the other half's MMAs.
+      // Iteration it: S (or S^T) and dP (or dP^T) as N = 128 products, each on
+      // its own barrier, so the element-wise warps form P while dP is still
+      // being computed; dK/dV: dV += P^T dO as soon as P is in TMEM (while
+      // the warps form dS), then dK += dS^T Q; dQ: dQ += dS K. The next tile's
+      // scores follow the accumulations (they overwrite the columns those
+      // read, in issue order).
       auto full = [&](int it) {  // both tiles of iteration it have landed (no fence)
         const int c0 = 2 * it, c1 = 2 * it + 1;
         return mbar_wait(bar(kBarFull + c0 % kStages), (c0 / kStages) & 1, abort_flag, err) &&
@@ -278,41 +279,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto ring0 = [&](int it) { return ring + ((2 * it) % kStages) * kTileBytes; };
       auto ring1 = [&](int it) { return ring + ((2 * it + 1) % kStages) * kTileBytes; };
-      auto scores = [&](int it, int h) {  // S = Q K_j^T, dP = dO V_j^T (or S^T = K Q_i^T, dP^T = V dO_i^T)
-        mma_rows_dot<D>(tS + 64 * h, stay0, ring0(it) + 8192 * h);
-        mma_rows_dot<D>(tDP + 64 * h, stay1, ring1(it) + 8192 * h);
-        mma_commit(bar(kBarSt + h));
+      auto scores = [&](int it) {  // S = Q K_j^T, dP = dO V_j^T (or S^T = K Q_i^T, dP^T = V dO_i^T)
+        mma_rows_dot<D>(tS, stay0, ring0(it));
+        mma_commit(bar(kBarSt));
+        mma_rows_dot<D>(tDP, stay1, ring1(it));
+        mma_commit(bar(kBarSt + 1));
       };
-      auto accumulate = [&](int it, int h) {
-        if (kDq) {
-          mma_acc_tmem<D>(tAcc0, tS, ring0(it), h, it == 0 && h == 0);   // dQ += dS K_j
-        } else {
-          mma_acc_tmem<D>(tAcc0, tS, ring1(it), h, it == 0 && h == 0);   // dV += P^T dO_i
-          mma_acc_tmem<D>(tAcc1, tDP, ring0(it), h, it == 0 && h == 0);  // dK += dS^T Q_i
-        }
-      };
-      // The issuing thread's waits, commits and fences stall the tensor pipe
-      // once its short queue drains, so they are gathered: one fence after
-      // the element-wise wait and the next tiles' arrival, then the half's
-      // accumulation and the next scores as one burst; one commit releases
-      // both ring slots of an iteration.
       bool ok = mbar_wait(bar(kBarStay), 0, abort_flag, err) && full(0);
-      tc_fence_after();
-      if (ok) {
-        scores(0, 0);
-        scores(0, 1);
-      }
+      if (ok) scores(0);
       for (int it = 0; ok && it < n_iter; ++it) {
         const bool more = it + 1 < n_iter;
-        if (!mbar_wait(bar(kBarPt), it & 1, abort_flag, err) || (more && !full(it + 1))) break;
+        if (!kDq) {  // dV += P^T dO_i
+          if (!mbar_wait(bar(kBarPt), it & 1, abort_flag, err)) break;
+          tc_fence_after();
+          mma_acc_tmem<D>(tAcc0, tS, ring1(it), 0, it == 0);
+          mma_acc_tmem<D>(tAcc0, tS, ring1(it), 1, false);
+        }
+        if (!mbar_wait(bar(kBarPt + 1), it & 1, abort_flag, err) || (more && !full(it + 1))) break;
         tc_fence_after();
-        accumulate(it, 0);
-        if (more) scores(it + 1, 0);
-        if (!mbar_wait(bar(kBarPt + 1), it & 1, abort_flag, err)) break;
-        tc_fence_after();
-        accumulate(it, 1);
+        if (kDq) {  // dQ += dS K_j
+          mma_acc_tmem<D>(tAcc0, tS, ring0(it), 0, it == 0);
+          mma_acc_tmem<D>(tAcc0, tS, ring0(it), 1, false);
+        } else {    // dK += dS^T Q_i
+          mma_acc_tmem<D>(tAcc1, tDP, ring0(it), 0, it == 0);
+          mma_acc_tmem<D>(tAcc1, tDP, ring0(it), 1, false);
+        }
         mma_commit(bar(kBarEmpty + it % (kStages / 2)));
-        if (more) scores(it + 1, 1);
+        if (more) scores(it + 1);
       }
       mma_commit(bar(kBarAcc));
       mbar_drain(bar(kBarAcc), 0, err);
@@ -362,70 +355,95 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int base = tile * kRows;
       const bool need_mask = base + kRows > S || srow + kRows > S ||
                              (p.causal && (kDq ? srow + kRows > base : srow < base + kRows));
-      bool got = ok && mbar_wait(bar(kBarSt + h), it & 1, abort_flag, err);
+      bool got = ok && mbar_wait(bar(kBarSt), it & 1, abort_flag, err);
       got = named_bar_and(1 + wg, 128, __all_sync(0xffffffffu, got));  // also publishes vec
       if (!got) break;
       tc_fence_after();
-      // 16 columns at col0: P and dS as bf16 pairs, written over the first 16
-      // of this warpgroup's columns (chunk c to c_base + 8c), which it has
-      // already read
-      auto chunk = [&](auto mask_tag, int c) {
+      // Phase 1, once S is in TMEM: P for this thread's 32 columns (kept in
+      // registers for dS); dK/dV writes it as bf16 pairs over the first 16 of
+      // the warpgroup's columns (chunk c to c_base + 8c), which it has read.
+      float pf[32];
+      auto chunk_p = [&](auto mask_tag, int c) {
         constexpr bool kMask = decltype(mask_tag)::value;
         const int col0 = c_base + 16 * c;
-        uint32_t sr[16], dr[16];
+        uint32_t sr[16];
         tmem_ld16(tS + lane_off + col0, sr);
-        tmem_ld16(tDP + lane_off + col0, dr);
-        float lv[16], dl[16];
+        float lv[16];
         if (!kDq) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const float4 a4 = reinterpret_cast<const float4 *>(vec + col0)[i];
-            const float4 d4 = reinterpret_cast<const float4 *>(vec + kRows + col0)[i];
             lv[4 * i] = a4.x, lv[4 * i + 1] = a4.y, lv[4 * i + 2] = a4.z, lv[4 * i + 3] = a4.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) lv[i] = row_lse2;
+        }
+        tmem_ld_wait(sr);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float pr = ex2_approx(__uint_as_float(sr[e]) * c2 - lv[e]);
+          if (kMask) {
+            const int other = srow + col0 + e;  // the query (dK/dV) or key (dQ) of this column
+            const int q_i = kDq ? my_row : other, k_j = kDq ? other : my_row;
+            if (!(q_i < S && k_j < S && (!p.causal || k_j <= q_i))) pr = 0.f;
+          }
+          pf[16 * c + e] = pr;
+        }
+        if (!kDq) {
+          uint32_t pa[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) pa[e] = pack_bf16x2(pf[16 * c + 2 * e], pf[16 * c + 2 * e + 1]);
+          tmem_st8(tS + lane_off + c_base + 8 * c, pa);  // P^T over S^T
+        }
+      };
+      if (need_mask) {
+        chunk_p(std::true_type{}, 0);
+        chunk_p(std::true_type{}, 1);
+      } else {
+        chunk_p(std::false_type{}, 0);
+        chunk_p(std::false_type{}, 1);
+      }
+      if (!kDq) {
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarPt));
+      }
+      // Phase 2, once dP is in TMEM: dS = P (dP - delta), as bf16 pairs over
+      // dP^T (dK/dV) or over S (dQ, where P never goes to TMEM)
+      got = mbar_wait(bar(kBarSt + 1), it & 1, abort_flag, err);
+      got = named_bar_and(1 + wg, 128, __all_sync(0xffffffffu, got));
+      if (!got) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int col0 = c_base + 16 * c;
+        uint32_t dr[16];
+        tmem_ld16(tDP + lane_off + col0, dr);
+        float dl[16];
+        if (!kDq) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float4 d4 = reinterpret_cast<const float4 *>(vec + kRows + col0)[i];
             dl[4 * i] = d4.x, dl[4 * i + 1] = d4.y, dl[4 * i + 2] = d4.z, dl[4 * i + 3] = d4.w;
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) lv[i] = row_lse2, dl[i] = row_delta;
+          for (int i = 0; i < 16; ++i) dl[i] = row_delta;
         }
-        tmem_ld_wait(sr);
         tmem_ld_wait(dr);
-        uint32_t pa[8], pb[8];
+        uint32_t pb[8];
 #pragma unroll
-        for (int e = 0; e < 16; e += 2) {
-          float pv[2], dsv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            float pr = ex2_approx(__uint_as_float(sr[e + u]) * c2 - lv[e + u]);
-            if (kMask) {
-              const int other = srow + col0 + e + u;  // the query (dK/dV) or key (dQ) of this column
-              const int q_i = kDq ? my_row : other, k_j = kDq ? other : my_row;
-              if (!(q_i < S && k_j < S && (!p.causal || k_j <= q_i))) pr = 0.f;
-            }
-            pv[u] = pr;
-            dsv[u] = pr * (__uint_as_float(dr[e + u]) - dl[e + u]);
-          }
-          pa[e / 2] = pack_bf16x2(pv[0], pv[1]);
-          pb[e / 2] = pack_bf16x2(dsv[0], dsv[1]);
-        }
-        if (kDq) {
-          tmem_st8(tS + lane_off + c_base + 8 * c, pb);  // dS over S
-        } else {
-          tmem_st8(tS + lane_off + c_base + 8 * c, pa);   // P^T over S^T
-          tmem_st8(tDP + lane_off + c_base + 8 * c, pb);  // dS^T over dP^T
-        }
-      };
-      if (need_mask) {
-        chunk(std::true_type{}, 0);
-        chunk(std::true_type{}, 1);
-      } else {
-        chunk(std::false_type{}, 0);
-        chunk(std::false_type{}, 1);
+        for (int e = 0; e < 8; ++e)
+          pb[e] = pack_bf16x2(pf[16 * c + 2 * e] * (__uint_as_float(dr[2 * e]) - dl[2 * e]),
+                              pf[16 * c + 2 * e + 1] * (__uint_as_float(dr[2 * e + 1]) - dl[2 * e + 1]));
+        tmem_st8((kDq ? tS : tDP) + lane_off + c_base + 8 * c, pb);  // dS (dQ) or dS^T over dP^T
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarPt + h));
+      if (lane == 0) mbar_arrive(bar(kBarPt + 1));
     }
     // ------------------------------------------------------------ epilogue
     bool done = ok && n_iter > 0 && mbar_wait(bar(kBarAcc), 0, abort_flag, err);

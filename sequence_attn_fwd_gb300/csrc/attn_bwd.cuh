@@ -19,8 +19,10 @@
 //               tiles stream through; S = Q K^T, dP = dO V^T, dS in TMEM, and
 //               dQ += dS K.
 // Both matrix kernels: warp 17 TMA producer, warp 16 MMA issuer (one thread),
-// warps 0-15 the element-wise pass (four warpgroups, two per 64-column half
-// of the tile, 32 columns each). Every wait is bounded.
+// warps 0-15 the element-wise pass (four warpgroups of 32 columns each, in
+// two phases per streamed tile: P from S, then dS from P and dP). The issuer
+// orders each tile's products so that one tile's element-wise phases overlap
+// its neighbours' products. Every wait is bounded.
 #pragma once
 #include <cuda_bf16.h>
 #include <math.h>
@@ -91,6 +93,18 @@ __device__ __forceinline__ void mma_acc_tmem(uint32_t acc, uint32_t a_tmem, uint
     mma_ts(acc, a_tmem + 64 * h + 32 * (k4 >> 1) + 8 * (k4 & 1), sw128_desc(b + kk * 2048, kColBlock, 1024), idesc,
            (first && k4 == 0) ? 0u : 1u);
   }
+}
+
+// acc (+)= A B over the full contraction of 128 elements, A = 128 x 128 bf16
+// in TMEM packed compactly (elements 16k..16k+15 in the 8 columns at
+// a_tmem + 8k), B as for mma_acc_tmem.
+template <int D>
+__device__ __forceinline__ void mma_acc_compact(uint32_t acc, uint32_t a_tmem, uint32_t b, bool first) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, D, true);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    mma_ts(acc, a_tmem + 8 * kk, sw128_desc(b + kk * 2048, kColBlock, 1024), idesc,
+           (first && kk == 0) ? 0u : 1u);
 }
 
 // NC columns of one thread's row of an fp32 TMEM accumulator, times `mul`,
@@ -225,6 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // TMEM: S or S^T [0,128) (then P / dS as bf16 pairs in columns [0,32) and [64,96)),
   // dP or dP^T [128,256), accumulators [256,256+D) and (dK/dV) [256+D,256+2D)
   const uint32_t tS = tmem, tDP = tmem + 128, tAcc0 = tmem + 256, tAcc1 = tmem + 256 + D;
+  const uint32_t tDS = tAcc1;  // dQ kernel: two 64-column buffers of packed dS (tAcc1 is dK/dV's)
 
   if (warp == kTmaWarp) {
     if (lane == 0 && !skip && n_iter > 0) {
@@ -268,10 +283,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t ring = smem_addr(sRing);
       // Iteration it: S (or S^T) and dP (or dP^T) as N = 128 products, each on
       // its own barrier, so the element-wise warps form P while dP is still
-      // being computed; dK/dV: dV += P^T dO as soon as P is in TMEM (while
-      // the warps form dS), then dK += dS^T Q; dQ: dQ += dS K. The next tile's
-      // scores follow the accumulations (they overwrite the columns those
-      // read, in issue order).
+      // being computed. dK/dV: dV += P^T dO as soon as P is in TMEM, then
+      // the next S (it overwrites P^T, in issue order behind dV), then
+      // dK += dS^T Q and the next dP. dQ: the next S as soon as the warps
+      // have read S out, dQ += dS K once dS is in TMEM (double-buffered in
+      // columns the dQ kernel has free), then the next dP. The element-wise
+      // pass of one tile thus overlaps the products of its neighbours.
       auto full = [&](int it) {  // both tiles of iteration it have landed (no fence)
         const int c0 = 2 * it, c1 = 2 * it + 1;
         return mbar_wait(bar(kBarFull + c0 % kStages), (c0 / kStages) & 1, abort_flag, err) &&
@@ -279,33 +296,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto ring0 = [&](int it) { return ring + ((2 * it) % kStages) * kTileBytes; };
       auto ring1 = [&](int it) { return ring + ((2 * it + 1) % kStages) * kTileBytes; };
-      auto scores = [&](int it) {  // S = Q K_j^T, dP = dO V_j^T (or S^T = K Q_i^T, dP^T = V dO_i^T)
+      // S = Q K_j^T, dP = dO V_j^T (or S^T = K Q_i^T, dP^T = V dO_i^T)
+      auto scores_s = [&](int it) {
         mma_rows_dot<D>(tS, stay0, ring0(it));
         mma_commit(bar(kBarSt));
+      };
+      auto scores_dp = [&](int it) {
         mma_rows_dot<D>(tDP, stay1, ring1(it));
         mma_commit(bar(kBarSt + 1));
       };
       bool ok = mbar_wait(bar(kBarStay), 0, abort_flag, err) && full(0);
-      if (ok) scores(0);
+      if (ok) {
+        scores_s(0);
+        scores_dp(0);
+      }
       for (int it = 0; ok && it < n_iter; ++it) {
         const bool more = it + 1 < n_iter;
+        // P^T in TMEM (dK/dV), or S read out (dQ); then the next S, which
+        // overwrites those columns, right behind the products that read them
+        if (!mbar_wait(bar(kBarPt), it & 1, abort_flag, err) || (more && !full(it + 1))) break;
+        tc_fence_after();
         if (!kDq) {  // dV += P^T dO_i
-          if (!mbar_wait(bar(kBarPt), it & 1, abort_flag, err)) break;
-          tc_fence_after();
           mma_acc_tmem<D>(tAcc0, tS, ring1(it), 0, it == 0);
           mma_acc_tmem<D>(tAcc0, tS, ring1(it), 1, false);
         }
-        if (!mbar_wait(bar(kBarPt + 1), it & 1, abort_flag, err) || (more && !full(it + 1))) break;
+        if (more) scores_s(it + 1);
+        if (!mbar_wait(bar(kBarPt + 1), it & 1, abort_flag, err)) break;
         tc_fence_after();
-        if (kDq) {  // dQ += dS K_j
-          mma_acc_tmem<D>(tAcc0, tS, ring0(it), 0, it == 0);
-          mma_acc_tmem<D>(tAcc0, tS, ring0(it), 1, false);
-        } else {    // dK += dS^T Q_i
+        if (kDq)  // dQ += dS K_j, dS in its own double-buffered columns
+          mma_acc_compact<D>(tAcc0, tDS + 64 * (it & 1), ring0(it), it == 0);
+        else {    // dK += dS^T Q_i
           mma_acc_tmem<D>(tAcc1, tDP, ring0(it), 0, it == 0);
           mma_acc_tmem<D>(tAcc1, tDP, ring0(it), 1, false);
         }
         mma_commit(bar(kBarEmpty + it % (kStages / 2)));
-        if (more) scores(it + 1);
+        if (more) scores_dp(it + 1);
       }
       mma_commit(bar(kBarAcc));
       mbar_drain(bar(kBarAcc), 0, err);
@@ -404,14 +429,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         chunk_p(std::false_type{}, 0);
         chunk_p(std::false_type{}, 1);
       }
-      if (!kDq) {
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarPt));
-      }
+      // P^T stored (dK/dV), or S read out (dQ): the issuer may overwrite S
+      if (!kDq) tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarPt));
       // Phase 2, once dP is in TMEM: dS = P (dP - delta), as bf16 pairs over
-      // dP^T (dK/dV) or over S (dQ, where P never goes to TMEM)
+      // dP^T (dK/dV) or into the iteration's dS buffer (dQ, where P never
+      // goes to TMEM)
       got = mbar_wait(bar(kBarSt + 1), it & 1, abort_flag, err);
       got = named_bar_and(1 + wg, 128, __all_sync(0xffffffffu, got));
       if (!got) break;
@@ -438,7 +463,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 8; ++e)
           pb[e] = pack_bf16x2(pf[16 * c + 2 * e] * (__uint_as_float(dr[2 * e]) - dl[2 * e]),
                               pf[16 * c + 2 * e + 1] * (__uint_as_float(dr[2 * e + 1]) - dl[2 * e + 1]));
-        tmem_st8((kDq ? tS : tDP) + lane_off + c_base + 8 * c, pb);  // dS (dQ) or dS^T over dP^T
+        if (kDq)  // dS packed compactly into the iteration's buffer (elements 16k.. at column 8k)
+          tmem_st8(tDS + 64 * (it & 1) + lane_off + (c_base / 16 + c) * 8, pb);
+        else      // dS^T over dP^T
+          tmem_st8(tDP + lane_off + c_base + 8 * c, pb);
       }
       tmem_st_wait();
       tc_fence_before();

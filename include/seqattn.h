@@ -235,7 +235,7 @@ int attn_fwd_fp8(const void *q8, const void *k8, const void *vt8, void *o, float
  *   lse         fp32 [B, Hq, S] from attn_fwd (natural log)
  *   delta       fp32 [B, Hq, S] workspace (written, then read)
  *   dq          bf16 [B, Hq, S, D];  dk, dv  bf16 [B, Hkv, S, D]  (outputs)
- * D in {64, 128} and S <= 65535 * 128 (else ATTN_ERR_UNSUPPORTED); bad
+ * D in {64, 128}, S <= 2^30 and B * Hq <= 65535 (else ATTN_ERR_UNSUPPORTED); bad
  * shapes, scale, pointers or alignment: ATTN_ERR_INVALID_ARG. Device pointers
  * owned by the caller; asynchronous on `stream`.
  */

@@ -245,8 +245,8 @@ int attn_bwd(const void *q, const void *k, const void *v, const void *o, const f
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
   if (!scale_ok(scale)) return ATTN_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
-  if (S > 65535ll * 128) return ATTN_ERR_UNSUPPORTED;  // 128-row tiles along the grid's y
-  if (static_cast<long long>(B) * Hq > 0x7fffffffll) return ATTN_ERR_UNSUPPORTED;
+  if (S > kMaxRowsPerHead) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Hq > 65535) return ATTN_ERR_UNSUPPORTED;  // heads along the grid's y
   if (B == 0 || S == 0) return ATTN_OK;
   const void *ptrs16[] = {q, k, v, o, dout, dq, dk, dv};
   for (const void *ptr : ptrs16)

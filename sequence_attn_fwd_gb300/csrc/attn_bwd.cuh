@@ -194,24 +194,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   int *err = &g_device_error;
   const int S = p.S, group = p.Hq / p.Hkv;
   const int n_tiles = (S + kRows - 1) / kRows;
-  // heads vary fastest and the CTAs with the most iterations come first: low
-  // key tiles (dK/dV), high query tiles (causal dQ)
-  const int head = blockIdx.x;  // b*Hkv + hkv (dK/dV) or b*Hq + hq (dQ)
-  const int tile = (kDq && p.causal) ? n_tiles - 1 - static_cast<int>(blockIdx.y)
-                                     : static_cast<int>(blockIdx.y);  // key or query tile
+  // tiles vary fastest, so the CTAs running together are tiles of one head
+  // (they stream the same tiles of that head's group, shared in L2); the CTAs
+  // with the most iterations come first: low key tiles (dK/dV), high query
+  // tiles (causal dQ)
+  const int head = blockIdx.y;  // b*Hkv + hkv (dK/dV) or b*Hq + hq (dQ)
+  const int tile = (kDq && p.causal) ? n_tiles - 1 - static_cast<int>(blockIdx.x)
+                                     : static_cast<int>(blockIdx.x);  // key or query tile
   const int b = kDq ? head / p.Hq : head / p.Hkv;
   // dK/dV: iterations over (query head of the group, query tile >= this key
   // tile when causal); dQ: over key tiles <= this query tile when causal
   const int first_stream = (!kDq && p.causal) ? tile : 0;
   const int n_stream_tiles = kDq ? (p.causal ? tile + 1 : n_tiles) : n_tiles - first_stream;
   const int n_iter = kDq ? n_stream_tiles : group * n_stream_tiles;
+  // dK/dV streams the query tiles from the last one down, the group's query
+  // heads innermost: every CTA of a KV head then reads the same (head, query
+  // tile) at the same iteration until it reaches its own diagonal, so the
+  // CTAs running together share each streamed tile in L2.
   auto stream_of = [&](int it, int &row, int &q_head) {  // the streamed tile of iteration it
     if (kDq) {
       row = it * kRows;
       q_head = head;
     } else {
-      row = (first_stream + it % n_stream_tiles) * kRows;
-      q_head = b * p.Hq + (head % p.Hkv) * group + it / n_stream_tiles;
+      row = (n_tiles - 1 - it / group) * kRows;
+      q_head = b * p.Hq + (head % p.Hkv) * group + it % group;
     }
   };
 

@@ -512,7 +512,7 @@ cudaError_t launch_bwd_typed(const CUtensorMap &tq, const CUtensorMap &tk, const
     auto kernel = dq ? bwd::attn_bwd_kernel<D, true> : bwd::attn_bwd_kernel<D, false>;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    const dim3 grid(static_cast<unsigned>(p.B * (dq ? p.Hq : p.Hkv)), n_tiles);
+    const dim3 grid(n_tiles, static_cast<unsigned>(p.B * (dq ? p.Hq : p.Hkv)));
     kernel<<<grid, bwd::kThreads, kSmem, stream>>>(tq, tk, tv, tdo, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

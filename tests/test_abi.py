@@ -180,7 +180,8 @@ def test_attn_bwd_argument_checks(lib):
 
     assert run(D=96) == 2 and run(D=32) == 2
     assert run(D=64, q=FAKE + 8) == 1  # D = 64 is accepted: it reaches the alignment checks
-    assert run(S=65536 * 128) == 2  # more than 65535 tiles of 128 rows
+    assert run(B=2, Hq=32768, Hkv=1) == 2  # more than 65535 (batch, query head) pairs
+    assert run(S=(1 << 30) + 128) == 2
     assert run(Hq=3, Hkv=2) == 1 and run(scale=-1.0) == 1
     assert run(q=FAKE + 8) == 1 and run(delta=FAKE + 2) == 1 and run(q=0) == 1
     assert run(S=0) == 0

@@ -367,8 +367,11 @@ __device__ __forceinline__ bool softmax_row(const AttnParams &p, const BlockDesc
         fence_proxy_async_shared();
         __syncwarp();
         if (wleader) {
-          tma_store_3d(store.map, wbuf, c * kChunkCols,
-                       static_cast<int>(blk.o_row + tile_first_row + warp_row0), store.head);
+          // O is written once and not read back by this kernel: let it leave
+          // L2 ahead of the K and V tiles other items still read
+          tma_store_3d_hint(store.map, wbuf, c * kChunkCols,
+                            static_cast<int>(blk.o_row + tile_first_row + warp_row0), store.head,
+                            l2_policy_evict_first());
           bulk_commit_group();
         }
       }

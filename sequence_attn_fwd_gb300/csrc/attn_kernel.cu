@@ -209,6 +209,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&tm_q);
       tma_prefetch_map(&tm_k);
       tma_prefetch_map(&tm_v);
+      // K and V are read again by every query block and head of their group:
+      // kept in L2 ahead of Q, which each item reads once
+      const uint64_t pol_keep = l2_policy_evict_last(), pol_stream = l2_policy_evict_first();
       int c = 0;   // K_0, V_0, K_1, V_1, ... of every item, in the order the MMA issuer consumes them
       int nq = 0;  // Q tile pairs loaded
       bool ok = true;
@@ -224,8 +227,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kv_row = static_cast<int>(blk.kv_row);
         for (int t = 0; t < 2; ++t)
           for (int cb = 0; cb < C::kColBlocks; ++cb)
-            tma_load_3d(smem_addr(sQ + (t * C::kColBlocks + cb) * kColBlockBytes), &tm_q,
-                        bar(kBarQFull), cb * C::kColBlockElems, q_row + t * kRowsPerTile, it.bh);
+            tma_load_3d_hint(smem_addr(sQ + (t * C::kColBlocks + cb) * kColBlockBytes), &tm_q,
+                             bar(kBarQFull), cb * C::kColBlockElems, q_row + t * kRowsPerTile, it.bh,
+                             pol_stream);
         ++nq;
         const int b = it.bh / p.Hq, hq = it.bh % p.Hq;
         const int kv_head = b * p.Hkv + hq / (p.Hq / p.Hkv);
@@ -240,14 +244,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(bar(kBarFull + slot), C::kTileBytes);
             if (kFp8 && which) {
               // V^T tile j: the 128 keys of the tile along x, all D rows (one box at D = 128)
-              tma_load_3d(smem_addr(sRing + slot * C::kTileBytes), &tm_v, bar(kBarFull + slot),
-                          kv_row + j * kRowsPerTile, 0, kv_head);
+              tma_load_3d_hint(smem_addr(sRing + slot * C::kTileBytes), &tm_v, bar(kBarFull + slot),
+                               kv_row + j * kRowsPerTile, 0, kv_head, pol_keep);
             } else {
               const CUtensorMap *map = which ? &tm_v : &tm_k;
               for (int cb = 0; cb < C::kColBlocks; ++cb)
-                tma_load_3d(smem_addr(sRing + (slot * C::kColBlocks + cb) * kColBlockBytes), map,
-                            bar(kBarFull + slot), cb * C::kColBlockElems, kv_row + j * kRowsPerTile,
-                            kv_head);
+                tma_load_3d_hint(smem_addr(sRing + (slot * C::kColBlocks + cb) * kColBlockBytes), map,
+                                 bar(kBarFull + slot), cb * C::kColBlockElems, kv_row + j * kRowsPerTile,
+                                 kv_head, pol_keep);
             }
           }
         }

@@ -12,7 +12,7 @@
 //   dK / dV     one CTA per 128-key tile of a (batch, KV head): K and V stay in
 //               shared memory while the query tiles of every query head of the
 //               GQA group stream through; S^T = K Q^T and dP^T = V dO^T land in
-//               TMEM, two warpgroups (64 query columns each) form P^T and dS^T
+//               TMEM, four warpgroups (32 query columns each) form P^T and dS^T
 //               as bf16 in TMEM, and dV += P^T dO, dK += dS^T Q accumulate in
 //               TMEM (TS form, Q and dO as N-contiguous operands).
 //   dQ          one CTA per 128-row query tile: Q and dO stay, the visible key

@@ -108,18 +108,19 @@ __device__ __forceinline__ BlockDesc block_of(const AttnParams &p, const SingleP
 __device__ __forceinline__ BlockDesc block_of(const AttnParams &, const BlockTable &tbl, int blk) {
   return tbl.b[blk];
 }
-__device__ __forceinline__ Item item_of(const AttnParams &p, const SingleProblem &, long long k) {
+__device__ __forceinline__ Item item_of(const AttnParams &p, const SingleProblem &, long long k, int &) {
   const long long heads = static_cast<long long>(p.B) * p.Hq;
   const int qi = static_cast<int>(k / heads);
   const int qblock = p.causal ? p.n_qblocks - 1 - qi : qi;
   return {0, static_cast<int>(k % heads), qblock * 2 * kRowsPerTile};
 }
-__device__ __forceinline__ Item item_of(const AttnParams &p, const BlockTable &tbl, long long k) {
-  int lo = 0, hi = tbl.n - 1;  // the last block with item_start <= k
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (tbl.item_start[mid] <= k) lo = mid; else hi = mid - 1;
-  }
+// `cur` is the caller's cursor: the block of its previous item. A CTA's items
+// come in increasing order, so the block of item k (the last one with
+// item_start <= k) is found by scanning on from there, usually in no step.
+__device__ __forceinline__ Item item_of(const AttnParams &p, const BlockTable &tbl, long long k, int &cur) {
+  int lo = cur;
+  while (lo + 1 < tbl.n && tbl.item_start[lo + 1] <= k) ++lo;
+  cur = lo;
   const long long local = k - tbl.item_start[lo];
   const long long heads = static_cast<long long>(p.B) * p.Hq;
   const int qi = static_cast<int>(local / heads);
@@ -215,8 +216,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int c = 0;   // K_0, V_0, K_1, V_1, ... of every item, in the order the MMA issuer consumes them
       int nq = 0;  // Q tile pairs loaded
       bool ok = true;
+      int cur_blk = 0;  // block of the previous item (block tables)
       for (long long i = 0, k = item_index(0); k < n_items && ok; k = item_index(++i)) {
-        const Item it = item_of(p, tbl, k);
+        const Item it = item_of(p, tbl, k, cur_blk);
         const int n_max = max(tiles(it, 0), tiles(it, 1));
         if (n_max == 0) continue;
         // the previous item's S MMAs must be done reading the Q buffer
@@ -284,8 +286,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g = 0;             // KV steps done by this tile over earlier items
       bool ok = true;
       int base = 0;          // burst slots of earlier items
+      int cur_blk = 0;  // block of the previous item (block tables)
       for (long long i = 0, k = item_index(0); k < n_items && ok; k = item_index(++i)) {
-        const Item it = item_of(p, tbl, k);
+        const Item it = item_of(p, tbl, k, cur_blk);
         const int nt = tiles(it, t);
         const int n_max = max(tiles(it, 0), tiles(it, 1));
         if (n_max == 0) continue;
@@ -386,8 +389,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t stage = smem_addr(sStage + t * C::kStageBytes);
     int g = 0;       // KV steps of this tile over earlier items
     uint32_t u = 0;  // earlier items in which this tile visited a KV tile
+    int cur_blk = 0;  // block of the previous item (block tables)
     for (long long i = 0, k = item_index(0); k < n_items; k = item_index(++i)) {
-      const Item it = item_of(p, tbl, k);
+      const Item it = item_of(p, tbl, k, cur_blk);
       const BlockDesc blk = block_of(p, tbl, it.blk);
       const int out_head = blk.part * p.B * p.Hq + it.bh;  // head of O / lse written
       const int tile_first = it.row0 + t * kRowsPerTile;

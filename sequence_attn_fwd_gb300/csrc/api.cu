@@ -83,6 +83,19 @@ bool make_out_map(CUtensorMap *map, void *base, int D, long long rows, long long
 
 bool scale_ok(float scale) { return isfinite(scale) && scale > 0.f; }
 
+// Heads per item chunk of a single problem: whole GQA groups whose K and V
+// (Skv rows each, elem_bytes per element) fit in 32 MB of L2 together, at
+// least one group.
+int heads_per_chunk(int B, int Hq, int Hkv, long long Skv, int D, int elem_bytes) {
+  const long long group = Hq / Hkv;
+  const long long kv_bytes = 2LL * (Skv > 0 ? Skv : 1) * D * elem_bytes;  // K and V of one KV head
+  long long groups = (32LL << 20) / kv_bytes;
+  if (groups < 1) groups = 1;
+  const long long heads = static_cast<long long>(B) * Hq;
+  const long long hc = groups * group;
+  return static_cast<int>(hc < heads ? hc : heads);
+}
+
 // 3-D byte view [heads][rows][cols] of e4m3 data (rows contiguous), box
 // 128 x 128 x 1 with 128-byte swizzle.
 bool make_map_u8(CUtensorMap *map, const void *base, long long cols, long long rows, long long heads) {
@@ -147,6 +160,7 @@ int run_attention(const void *q, const void *k, const void *v, long long q_off, 
   p.skip_empty = skip_empty ? 1 : 0;
   p.o_rows = Sq;
   p.o_scale = 1.f;
+  p.heads_per_chunk = heads_per_chunk(B, Hq, Hkv, Skv, D, 2);
   cudaError_t e = seqattn::launch_attention(D, f32_out, tq, tk, tv, to, p, stream);
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
@@ -313,6 +327,7 @@ int attn_fwd_fp8(const void *q8, const void *k8, const void *vt8, void *o, float
   p.skip_empty = 0;
   p.o_rows = S;
   p.o_scale = v_scale;
+  p.heads_per_chunk = heads_per_chunk(B, Hq, Hkv, S, D, 1);
   cudaError_t e = seqattn::launch_attention_fp8(tq, tk, tvt, to, p, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }

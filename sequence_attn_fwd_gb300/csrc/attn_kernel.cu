@@ -96,9 +96,6 @@ struct SingleProblem {
   int unused;
 };
 
-__device__ __forceinline__ long long n_items_of(const AttnParams &p, const SingleProblem &) {
-  return static_cast<long long>(p.B) * p.Hq * p.n_qblocks;
-}
 __device__ __forceinline__ long long n_items_of(const AttnParams &, const BlockTable &tbl) {
   return tbl.item_start[tbl.n];
 }
@@ -108,11 +105,38 @@ __device__ __forceinline__ BlockDesc block_of(const AttnParams &p, const SingleP
 __device__ __forceinline__ BlockDesc block_of(const AttnParams &, const BlockTable &tbl, int blk) {
   return tbl.b[blk];
 }
+// Single problems: the heads come in chunks of p.heads_per_chunk (whole GQA
+// groups, sized on the host so that a chunk's K and V stay in L2), and within
+// a chunk the items are numbered with the head fastest, so that the query
+// heads of a KV head run side by side and every K / V tile is read from DRAM
+// about once. Every chunk but the last is padded with empty items to whole
+// rounds of gridDim.x, so that a chunk's light last items and the next
+// chunk's heavy first ones never share a round (the padding items have no
+// rows: every role skips them).
+__device__ __forceinline__ long long chunk_items(const AttnParams &p, long long heads, long long &hc) {
+  hc = p.heads_per_chunk > 0 && p.heads_per_chunk < heads ? p.heads_per_chunk : heads;
+  const long long G = gridDim.x;
+  return (hc * p.n_qblocks + G - 1) / G * G;  // a full chunk's items with its padding
+}
+__device__ __forceinline__ long long n_items_of(const AttnParams &p, const SingleProblem &) {
+  const long long heads = static_cast<long long>(p.B) * p.Hq;
+  long long hc;
+  const long long per_chunk = chunk_items(p, heads, hc);
+  const long long n_chunks = (heads + hc - 1) / hc;
+  return (n_chunks - 1) * per_chunk + (heads - (n_chunks - 1) * hc) * p.n_qblocks;
+}
 __device__ __forceinline__ Item item_of(const AttnParams &p, const SingleProblem &, long long k, int &) {
   const long long heads = static_cast<long long>(p.B) * p.Hq;
-  const int qi = static_cast<int>(k / heads);
+  long long hc;
+  const long long per_chunk = chunk_items(p, heads, hc);
+  const long long c = k / per_chunk;
+  const long long h0 = c * hc;
+  const long long hn = heads - h0 < hc ? heads - h0 : hc;  // the last chunk may be short
+  const long long r = k - c * per_chunk;
+  if (r >= hn * p.n_qblocks) return {0, 0, p.n_qblocks * 2 * kRowsPerTile};  // padding: no rows
+  const int qi = static_cast<int>(r / hn);
   const int qblock = p.causal ? p.n_qblocks - 1 - qi : qi;
-  return {0, static_cast<int>(k % heads), qblock * 2 * kRowsPerTile};
+  return {0, static_cast<int>(h0 + r % hn), qblock * 2 * kRowsPerTile};
 }
 // `cur` is the caller's cursor: the block of its previous item. A CTA's items
 // come in increasing order, so the block of item k (the last one with

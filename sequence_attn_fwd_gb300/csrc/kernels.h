@@ -19,6 +19,8 @@ struct AttnParams {
   int skip_empty;     // rows that see no key: write lse = -inf only, leave O untouched
   long long o_rows;   // rows per head of O and lse (Sq for a single problem)
   float o_scale;      // e4m3 attention: the V scale applied to O (1 otherwise)
+  int heads_per_chunk;  // single problems: items come in chunks of this many consecutive
+                        // heads (whole GQA groups), all query blocks of a chunk before the next
 };
 
 // One block of attention: the queries in rows [q_row, q_row + Sq) of Q (per

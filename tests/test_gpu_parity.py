@@ -305,6 +305,35 @@ def test_ring_grouped_launch_is_bitwise_the_per_chunk_launches(sa):
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+@pytest.mark.parametrize("D,Hq,Hkv", [(128, 8, 4), (64, 16, 8)])
+def test_single_problem_head_chunks_cover_every_row(sa, D, Hq, Hkv):
+    """At S = 32768 a single problem's items come in chunks of whole GQA groups
+    whose K and V fit in 32 MB of L2 (two chunks in both cases), every chunk
+    but the last padded with empty items to whole rounds of the grid. The same
+    attention through the block-table launch (one block, items not chunked)
+    must give bitwise the same fp32 partials and lse on every row; both
+    outputs start as NaN, so a row that no item wrote fails. A few rows per
+    head are also checked against the oracle."""
+    S = 32768
+    w = adhoc(1, Hq, Hkv, S, D, True, seed=91)
+    q, k, v = workloads.make_qkv(w)
+    qd, kd, vd = to_dev(q, k, v)
+    nan = float("nan")
+    o1 = torch.full((1, Hq, S, D), nan, device="cuda")
+    l1 = torch.full((1, Hq, S), nan, device="cuda")
+    sa.attn_partial(qd, kd, vd, 0, 0, True, out=o1, lse=l1)
+    o2 = torch.full((1, 1, Hq, S, D), nan, device="cuda")
+    l2 = torch.full((1, 1, Hq, S), nan, device="cuda")
+    sa.attn_partial_blocks(qd, kd, vd, [(0, 0, 0, 0, 0, S, S, 0)], n_parts=1, causal=True, out=o2, lse=l2)
+    torch.cuda.synchronize()
+    sa.query_device_error()
+    assert torch.equal(o1, o2[0]) and torch.equal(l1, l2[0])
+    rows = workloads.sample_query_rows(w, n=4)
+    o_ref, lse_ref = oracle.attention(q, k, v, True, rows=rows)
+    check_o(gather_rows(o1, rows), o_ref, bf16_out=False)
+    check_lse(gather_rows(l1, rows), lse_ref)
+
+
 @pytest.mark.parametrize("shape", [(1, 2, 2, 512, True), (1, 4, 2, 1008, True), (2, 2, 1, 384, False)],
                          ids=["s512c", "gqa_s1008c", "b2_s384"])
 def test_attn_fwd_fp8_against_oracle(sa, shape):

@@ -49,6 +49,9 @@ METRIC = "attention fwd TFLOP/s (causal-adjusted) & % BF16 peak; lse_merge GB/s 
 METRIC_BWD = "attention bwd TFLOP/s (causal-adjusted, 2.5x the forward's FLOPs) & % BF16 peak"
 DEFAULT_WORKLOAD = "ring16_b1hq32hkv8s131072d128_causal"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# A step this long keeps the GPU at its power cap the way the sustained GEMM
+# loop of the peaks does: its kernels are held to the sustained peak.
+LONG_STEP_MS = 50.0
 L2_BYTES = 129e6
 
 
@@ -367,13 +370,21 @@ def run_ours(args, w: workloads.Workload, rank: int, world: int):
             "attn_partial": "<f32 out> (attn_partial)", "attn_fwd": "<bf16 out>",
             "attn_fwd_varlen": f"<bf16 out> (attn_fwd_varlen: {len(cu) - 1 if cu else 0} packed sequences)",
             "attn_fwd_fp8": "<bf16 out, e4m3 Q/K/V/P> (attn_fwd_fp8)"}[entry]
-    # e4m3 MMAs: the measured bf16 peak times the nominal e4m3 / bf16 ratio (4.5 / 2.25)
-    peak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
+    # The burst peak for a kernel timed alone; the sustained one (a seconds-long
+    # GEMM loop under the power cap) for a kernel inside a long step, here the
+    # partials launch of a step of LONG_STEP_MS or more, which runs as long as
+    # that loop does. e4m3 MMAs: the measured bf16 peak times the nominal
+    # e4m3 / bf16 ratio (4.5 / 2.25).
+    sustained = ms_per_step >= LONG_STEP_MS
+    bf16_peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+    peak = bf16_peak * (2.0 if fp8 else 1.0)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak,
                 "traffic": measured_traffic(entry, w.name),
                 "kernel": f"attn_fwd_kernel<{D}>" + what,
-                "peak_source": f"{peak_src} bf16 burst" + (" x 2 (nominal e4m3 / bf16 ratio)" if fp8 else ""),
+                "peak_source": (f"{peak_src} bf16 sustained (a {ms_per_step:.0f} ms step)" if sustained
+                                else f"{peak_src} bf16 burst") + (" x 2 (nominal e4m3 / bf16 ratio)" if fp8 else ""),
+                "frac_of_burst": achieved / (peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)),
                 "launch_ms": attn_avg_ms}
     merge = None
     if merge_ms:

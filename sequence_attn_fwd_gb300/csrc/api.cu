@@ -192,6 +192,29 @@ int run_blocks(const void *q, const void *k, const void *v, void *o, float *lse,
   p.skip_empty = skip_empty ? 1 : 0;
   p.o_rows = o_rows;
   p.o_scale = 1.f;
+  // Short blocks that all share their query rows (the key chunks of a ring
+  // pass, up to kSegMaxKeys keys each) run as the segments of each work item:
+  // Q is loaded once for all of them and each chunk's first scores follow the
+  // previous chunk's last product, which pays where an item's fixed cost is a
+  // large part of its work. Longer chunks keep the block table, whose items
+  // run one chunk after another and so keep a chunk's K and V in L2, where
+  // segments would stream the K and V of every chunk at once.
+  constexpr int kSegMaxKeys = 2048;
+  bool shared_q = blocks.size() >= 2 && blocks[0].Sq > 0;
+  for (const auto &b : blocks)
+    shared_q = shared_q && b.q_row == blocks[0].q_row && b.o_row == blocks[0].o_row &&
+               b.q_pos == blocks[0].q_pos && b.Sq == blocks[0].Sq && b.Skv <= kSegMaxKeys;
+  if (shared_q) {
+    for (size_t first = 0; first < blocks.size(); first += seqattn::kMaxLaunchBlocks) {
+      seqattn::SegTable tbl{};
+      const size_t n = std::min(blocks.size() - first, static_cast<size_t>(seqattn::kMaxLaunchBlocks));
+      tbl.n = static_cast<int>(n);
+      for (size_t i = 0; i < n; ++i) tbl.b[i] = blocks[first + i];
+      cudaError_t e = seqattn::launch_attention_segments(D, f32_out, tq, tk, tv, to, p, tbl, stream);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return ATTN_OK;
+  }
   for (size_t first = 0; first < blocks.size(); first += seqattn::kMaxLaunchBlocks) {
     seqattn::BlockTable tbl{};
     const size_t n = std::min(blocks.size() - first, static_cast<size_t>(seqattn::kMaxLaunchBlocks));

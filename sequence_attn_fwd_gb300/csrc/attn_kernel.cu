@@ -38,6 +38,8 @@
 
 #include <atomic>
 
+#include <type_traits>
+
 #include "attn_common.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -152,6 +154,32 @@ __device__ __forceinline__ Item item_of(const AttnParams &p, const BlockTable &t
   const int qblock = p.causal ? n_qb - 1 - qi : qi;
   return {lo, static_cast<int>(local % heads), qblock * 2 * kRowsPerTile};
 }
+// Blocks sharing their query rows: items number 256-row query blocks of the
+// shared rows with the head fastest, longest first when causal; every block
+// of the table is a segment of each item.
+__device__ __forceinline__ long long n_items_of(const AttnParams &p, const SegTable &tbl) {
+  return static_cast<long long>(p.B) * p.Hq * ((tbl.b[0].Sq + 2 * kRowsPerTile - 1) / (2 * kRowsPerTile));
+}
+__device__ __forceinline__ Item item_of(const AttnParams &p, const SegTable &tbl, long long k, int &) {
+  const long long heads = static_cast<long long>(p.B) * p.Hq;
+  const int qi = static_cast<int>(k / heads);
+  const int n_qb = (tbl.b[0].Sq + 2 * kRowsPerTile - 1) / (2 * kRowsPerTile);
+  const int qblock = p.causal ? n_qb - 1 - qi : qi;
+  return {0, static_cast<int>(k % heads), qblock * 2 * kRowsPerTile};
+}
+// Segments of an item: one (its block) except with a SegTable.
+__device__ __forceinline__ int n_segs_of(const SingleProblem &) { return 1; }
+__device__ __forceinline__ int n_segs_of(const BlockTable &) { return 1; }
+__device__ __forceinline__ int n_segs_of(const SegTable &tbl) { return tbl.n; }
+__device__ __forceinline__ BlockDesc seg_block(const AttnParams &p, const SingleProblem &t, const Item &, int) {
+  return block_of(p, t, 0);
+}
+__device__ __forceinline__ BlockDesc seg_block(const AttnParams &p, const BlockTable &t, const Item &it, int) {
+  return block_of(p, t, it.blk);
+}
+__device__ __forceinline__ BlockDesc seg_block(const AttnParams &, const SegTable &t, const Item &, int s) {
+  return t.b[s];
+}
 
 // kFp8: Q, K in e4m3 with K-major tiles, V given transposed ([heads][D][keys],
 // so its tiles are K-major too), P rounded to e4m3 in TMEM (one instantiation:
@@ -215,19 +243,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const bool skip = *abort_flag != 0;
-  // KV tiles query tile t of an item visits (0: none of its rows sees a key)
-  auto tiles = [&](const Item &it, int t) -> int {
-    return skip ? 0 : kv_tiles_for(block_of(p, tbl, it.blk), p.causal, it.row0 + t * kRowsPerTile);
+  // Single problems and block tables take the loops without segments (one a
+  // work item); tables of blocks sharing their query rows the segmented ones.
+  constexpr bool kSeg = std::is_same<Table, SegTable>::value;
+  static_assert(!(kSeg && kFp8), "segmented items load V in the bf16 layout only");
+  const int n_segs = n_segs_of(tbl);
+  // KV tiles query tile t of an item visits in segment sg (0: none of its rows sees a key)
+  auto tiles = [&](const Item &it, int sg, int t) -> int {
+    return skip ? 0 : kv_tiles_for(seg_block(p, tbl, it, sg), p.causal, it.row0 + t * kRowsPerTile);
   };
+  auto seg_max = [&](const Item &it, int sg) { return max(tiles(it, sg, 0), tiles(it, sg, 1)); };
   // TMEM column of S_t / P_t and of O_t for query tile t
   auto tS = [&](int t) -> uint32_t { return tmem + 128u * static_cast<uint32_t>(t); };
   auto tO = [&](int t) -> uint32_t { return tmem + 256u + 128u * static_cast<uint32_t>(t); };
 
   // The CTA works through items item_index(0), item_index(1), ...; each role
-  // walks the same sequence and skips the items with no visible key.
-  // Barrier phases run on across items: the Q buffer by loaded item, the K/V
-  // ring by ring position, S/P by KV step of each query tile, O by item of
-  // each query tile.
+  // walks the same sequence, and within an item its segments (one, except
+  // with a SegTable), and skips those with no visible key. Barrier phases run
+  // on across items: the Q buffer by loaded item, the K/V ring by ring
+  // position, S/P by KV step of each query tile, O by segment of each query
+  // tile.
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && !skip) {
@@ -240,44 +275,86 @@ __global__ void __launch_bounds__(kThreads, 1)
       int c = 0;   // K_0, V_0, K_1, V_1, ... of every item, in the order the MMA issuer consumes them
       int nq = 0;  // Q tile pairs loaded
       bool ok = true;
-      int cur_blk = 0;  // block of the previous item (block tables)
-      for (long long i = 0, k = item_index(0); k < n_items && ok; k = item_index(++i)) {
-        const Item it = item_of(p, tbl, k, cur_blk);
-        const int n_max = max(tiles(it, 0), tiles(it, 1));
-        if (n_max == 0) continue;
-        // the previous item's S MMAs must be done reading the Q buffer
-        if (nq > 0 && !mbar_wait(bar(kBarQEmpty), (nq - 1) & 1, abort_flag, err)) break;
-        mbar_arrive_expect_tx(bar(kBarQFull), 2 * C::kTileBytes);
-        const BlockDesc blk = block_of(p, tbl, it.blk);
-        const int q_row = static_cast<int>(blk.q_row) + it.row0;
-        const int kv_row = static_cast<int>(blk.kv_row);
-        for (int t = 0; t < 2; ++t)
-          for (int cb = 0; cb < C::kColBlocks; ++cb)
-            tma_load_3d_hint(smem_addr(sQ + (t * C::kColBlocks + cb) * kColBlockBytes), &tm_q,
-                             bar(kBarQFull), cb * C::kColBlockElems, q_row + t * kRowsPerTile, it.bh,
-                             pol_stream);
-        ++nq;
-        const int b = it.bh / p.Hq, hq = it.bh % p.Hq;
-        const int kv_head = b * p.Hkv + hq / (p.Hq / p.Hkv);
-        for (int j = 0; j < n_max && ok; ++j) {
-          for (int which = 0; which < 2; ++which, ++c) {
-            const int slot = c % C::kStages;
-            if (c >= C::kStages &&
-                !mbar_wait(bar(kBarEmpty + slot), ((c / C::kStages) - 1) & 1, abort_flag, err)) {
-              ok = false;
-              break;
+      if constexpr (!kSeg) {
+        int cur_blk = 0;  // block of the previous item (block tables)
+        for (long long i = 0, k = item_index(0); k < n_items && ok; k = item_index(++i)) {
+          const Item it = item_of(p, tbl, k, cur_blk);
+          const int n_max = seg_max(it, 0);
+          if (n_max == 0) continue;
+          // the previous item's S MMAs must be done reading the Q buffer
+          if (nq > 0 && !mbar_wait(bar(kBarQEmpty), (nq - 1) & 1, abort_flag, err)) break;
+          mbar_arrive_expect_tx(bar(kBarQFull), 2 * C::kTileBytes);
+          const BlockDesc blk = block_of(p, tbl, it.blk);
+          const int q_row = static_cast<int>(blk.q_row) + it.row0;
+          const int kv_row = static_cast<int>(blk.kv_row);
+          for (int t = 0; t < 2; ++t)
+            for (int cb = 0; cb < C::kColBlocks; ++cb)
+              tma_load_3d_hint(smem_addr(sQ + (t * C::kColBlocks + cb) * kColBlockBytes), &tm_q,
+                               bar(kBarQFull), cb * C::kColBlockElems, q_row + t * kRowsPerTile, it.bh,
+                               pol_stream);
+          ++nq;
+          const int b = it.bh / p.Hq, hq = it.bh % p.Hq;
+          const int kv_head = b * p.Hkv + hq / (p.Hq / p.Hkv);
+          for (int j = 0; j < n_max && ok; ++j) {
+            for (int which = 0; which < 2; ++which, ++c) {
+              const int slot = c % C::kStages;
+              if (c >= C::kStages &&
+                  !mbar_wait(bar(kBarEmpty + slot), ((c / C::kStages) - 1) & 1, abort_flag, err)) {
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(bar(kBarFull + slot), C::kTileBytes);
+              if (kFp8 && which) {
+                // V^T tile j: the 128 keys of the tile along x, all D rows (one box at D = 128)
+                tma_load_3d_hint(smem_addr(sRing + slot * C::kTileBytes), &tm_v, bar(kBarFull + slot),
+                                 kv_row + j * kRowsPerTile, 0, kv_head, pol_keep);
+              } else {
+                const CUtensorMap *map = which ? &tm_v : &tm_k;
+                for (int cb = 0; cb < C::kColBlocks; ++cb)
+                  tma_load_3d_hint(smem_addr(sRing + (slot * C::kColBlocks + cb) * kColBlockBytes), map,
+                                   bar(kBarFull + slot), cb * C::kColBlockElems, kv_row + j * kRowsPerTile,
+                                   kv_head, pol_keep);
+              }
             }
-            mbar_arrive_expect_tx(bar(kBarFull + slot), C::kTileBytes);
-            if (kFp8 && which) {
-              // V^T tile j: the 128 keys of the tile along x, all D rows (one box at D = 128)
-              tma_load_3d_hint(smem_addr(sRing + slot * C::kTileBytes), &tm_v, bar(kBarFull + slot),
-                               kv_row + j * kRowsPerTile, 0, kv_head, pol_keep);
-            } else {
-              const CUtensorMap *map = which ? &tm_v : &tm_k;
-              for (int cb = 0; cb < C::kColBlocks; ++cb)
-                tma_load_3d_hint(smem_addr(sRing + (slot * C::kColBlocks + cb) * kColBlockBytes), map,
-                                 bar(kBarFull + slot), cb * C::kColBlockElems, kv_row + j * kRowsPerTile,
-                                 kv_head, pol_keep);
+          }
+        }
+      } else {
+        int cur_blk = 0;  // block of the previous item (block tables)
+        for (long long i = 0, k = item_index(0); k < n_items && ok; k = item_index(++i)) {
+          const Item it = item_of(p, tbl, k, cur_blk);
+          bool any = false;
+          for (int sg = 0; sg < n_segs && !any; ++sg) any = seg_max(it, sg) > 0;
+          if (!any) continue;
+          // the previous item's S MMAs must be done reading the Q buffer
+          if (nq > 0 && !mbar_wait(bar(kBarQEmpty), (nq - 1) & 1, abort_flag, err)) break;
+          mbar_arrive_expect_tx(bar(kBarQFull), 2 * C::kTileBytes);
+          const int q_row = static_cast<int>(seg_block(p, tbl, it, 0).q_row) + it.row0;
+          for (int t = 0; t < 2; ++t)
+            for (int cb = 0; cb < C::kColBlocks; ++cb)
+              tma_load_3d_hint(smem_addr(sQ + (t * C::kColBlocks + cb) * kColBlockBytes), &tm_q,
+                               bar(kBarQFull), cb * C::kColBlockElems, q_row + t * kRowsPerTile, it.bh,
+                               pol_stream);
+          ++nq;
+          const int b = it.bh / p.Hq, hq = it.bh % p.Hq;
+          const int kv_head = b * p.Hkv + hq / (p.Hq / p.Hkv);
+          for (int sg = 0; sg < n_segs && ok; ++sg) {  // each segment's K/V tiles in turn
+            const int n_max = seg_max(it, sg);
+            const int kv_row = static_cast<int>(seg_block(p, tbl, it, sg).kv_row);
+            for (int j = 0; j < n_max && ok; ++j) {
+              for (int which = 0; which < 2; ++which, ++c) {
+                const int slot = c % C::kStages;
+                if (c >= C::kStages &&
+                    !mbar_wait(bar(kBarEmpty + slot), ((c / C::kStages) - 1) & 1, abort_flag, err)) {
+                  ok = false;
+                  break;
+                }
+                mbar_arrive_expect_tx(bar(kBarFull + slot), C::kTileBytes);
+                const CUtensorMap *map = which ? &tm_v : &tm_k;
+                for (int cb = 0; cb < C::kColBlocks; ++cb)
+                  tma_load_3d_hint(smem_addr(sRing + (slot * C::kColBlocks + cb) * kColBlockBytes), map,
+                                   bar(kBarFull + slot), cb * C::kColBlockElems, kv_row + j * kRowsPerTile,
+                                   kv_head, pol_keep);
+              }
             }
           }
         }
@@ -310,94 +387,195 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g = 0;             // KV steps done by this tile over earlier items
       bool ok = true;
       int base = 0;          // burst slots of earlier items
-      int cur_blk = 0;  // block of the previous item (block tables)
-      for (long long i = 0, k = item_index(0); k < n_items && ok; k = item_index(++i)) {
-        const Item it = item_of(p, tbl, k, cur_blk);
-        const int nt = tiles(it, t);
-        const int n_max = max(tiles(it, 0), tiles(it, 1));
-        if (n_max == 0) continue;
-        if (!mbar_wait(bar(kBarQFull), nq & 1, abort_flag, err)) break;
-        ++nq;
-        if (nt == 0) mma_commit(bar(kBarQEmpty));  // this tile reads nothing of Q
-        // Burst slots alternate between the tiles: (step j, tile t) is slot
-        // base + 2 j + t. A tile waits for its data before its slot comes up
-        // and makes its commits after handing the slot on, so that its
-        // waits and commits overlap the other tile's MMAs.
-        for (int j = 0; ok && j <= n_max; ++j) {
-          const int cK = c + 2 * j, cV = c + 2 * j - 1;  // ring positions of K_j and V_{j-1}
-          const int sK = cK % C::kStages, sV = (cV + C::kStages) % C::kStages;
-          const int cV2 = cK + 1, sV2 = cV2 % C::kStages;  // V_j
-          const uint32_t k_base = ring_base + sK * C::kTileBytes;
-          const uint32_t v_base = ring_base + sV * C::kTileBytes;
-          const bool has_pv = j >= 1 && j - 1 < nt, has_s = j < nt, unused = !has_s && j < n_max;
-          // the data first (usually there already), the softmax's P last
-          if ((has_s || unused) && !mbar_wait(bar(kBarFull + sK), (cK / C::kStages) & 1, abort_flag, err)) {
-            ok = false;
-            break;
-          }
-          if (unused && !mbar_wait(bar(kBarFull + sV2), (cV2 / C::kStages) & 1, abort_flag, err)) {
-            ok = false;
-            break;
-          }
-          if (has_pv && (!mbar_wait(bar(kBarFull + sV), (cV / C::kStages) & 1, abort_flag, err) ||
-                         !mbar_wait(bar(kBarPFull + t), (g + j - 1) & 1, abort_flag, err))) {
-            ok = false;
-            break;
-          }
-          const int slot = base + 2 * j + t;
-          if (!wait_turn(turn, slot, abort_flag, err)) {
-            ok = false;
-            break;
-          }
-          if (has_pv) {
-            // O_t += P_t V_{j-1}; P_t was written over S_t by the softmax
-            // warps. For j = 1 this overwrites O_t: the warpgroup read the
-            // previous item's O_t before it signalled this P.
-            tc_fence_after();
-            if constexpr (kFp8) {
+      if constexpr (!kSeg) {
+        int cur_blk = 0;  // block of the previous item (block tables)
+        for (long long i = 0, k = item_index(0); k < n_items && ok; k = item_index(++i)) {
+          const Item it = item_of(p, tbl, k, cur_blk);
+          const int nt = tiles(it, 0, t);
+          const int n_max = seg_max(it, 0);
+          if (n_max == 0) continue;
+          if (!mbar_wait(bar(kBarQFull), nq & 1, abort_flag, err)) break;
+          ++nq;
+          if (nt == 0) mma_commit(bar(kBarQEmpty));  // this tile reads nothing of Q
+          // Burst slots alternate between the tiles: (step j, tile t) is slot
+          // base + 2 j + t. A tile waits for its data before its slot comes up
+          // and makes its commits after handing the slot on, so that its
+          // waits and commits overlap the other tile's MMAs.
+          for (int j = 0; ok && j <= n_max; ++j) {
+            const int cK = c + 2 * j, cV = c + 2 * j - 1;  // ring positions of K_j and V_{j-1}
+            const int sK = cK % C::kStages, sV = (cV + C::kStages) % C::kStages;
+            const int cV2 = cK + 1, sV2 = cV2 % C::kStages;  // V_j
+            const uint32_t k_base = ring_base + sK * C::kTileBytes;
+            const uint32_t v_base = ring_base + sV * C::kTileBytes;
+            const bool has_pv = j >= 1 && j - 1 < nt, has_s = j < nt, unused = !has_s && j < n_max;
+            // the data first (usually there already), the softmax's P last
+            if ((has_s || unused) && !mbar_wait(bar(kBarFull + sK), (cK / C::kStages) & 1, abort_flag, err)) {
+              ok = false;
+              break;
+            }
+            if (unused && !mbar_wait(bar(kBarFull + sV2), (cV2 / C::kStages) & 1, abort_flag, err)) {
+              ok = false;
+              break;
+            }
+            if (has_pv && (!mbar_wait(bar(kBarFull + sV), (cV / C::kStages) & 1, abort_flag, err) ||
+                           !mbar_wait(bar(kBarPFull + t), (g + j - 1) & 1, abort_flag, err))) {
+              ok = false;
+              break;
+            }
+            const int slot = base + 2 * j + t;
+            if (!wait_turn(turn, slot, abort_flag, err)) {
+              ok = false;
+              break;
+            }
+            if (has_pv) {
+              // O_t += P_t V_{j-1}; P_t was written over S_t by the softmax
+              // warps. For j = 1 this overwrites O_t: the warpgroup read the
+              // previous item's O_t before it signalled this P.
+              tc_fence_after();
+              if constexpr (kFp8) {
 #pragma unroll
-              for (int kk = 0; kk < kRowsPerTile / 32; ++kk)
-                mma_ts_e4m3(o_col, s_col + kk * 8, sw128_desc(v_base + kk * 32, 16, 1024), idesc_o,
-                            (j > 1 || kk > 0) ? 1u : 0u);
-            } else {
-              // descriptor start fields advance by 2048 / 16 per 16 keys
-              const uint64_t vd = sw128_desc(v_base, kColBlockBytes, 1024);
-              mma_ts(o_col, s_col, vd, idesc_o, j > 1 ? 1u : 0u);
+                for (int kk = 0; kk < kRowsPerTile / 32; ++kk)
+                  mma_ts_e4m3(o_col, s_col + kk * 8, sw128_desc(v_base + kk * 32, 16, 1024), idesc_o,
+                              (j > 1 || kk > 0) ? 1u : 0u);
+              } else {
+                // descriptor start fields advance by 2048 / 16 per 16 keys
+                const uint64_t vd = sw128_desc(v_base, kColBlockBytes, 1024);
+                mma_ts(o_col, s_col, vd, idesc_o, j > 1 ? 1u : 0u);
 #pragma unroll
-              for (int kk = 1; kk < kRowsPerTile / 16; ++kk)
-                mma_ts(o_col, s_col + kk * 8, vd + static_cast<uint64_t>(kk * 128), idesc_o, 1u);
+                for (int kk = 1; kk < kRowsPerTile / 16; ++kk)
+                  mma_ts(o_col, s_col + kk * 8, vd + static_cast<uint64_t>(kk * 128), idesc_o, 1u);
+              }
+            }
+            if (has_s) {
+              // S_t = Q_t K_j^T
+              const uint64_t qd = sw128_desc(qt, 16, 1024), kd = sw128_desc(k_base, 16, 1024);
+#pragma unroll
+              for (int kk = 0; kk < kKSteps; ++kk) {
+                const uint64_t off = static_cast<uint64_t>(((kk / 4) * kColBlockBytes + (kk % 4) * 32) >> 4);
+                if constexpr (kFp8)
+                  mma_ss_e4m3(s_col, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+                else
+                  mma_ss(s_col, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+              }
+            }
+            *turn = slot + 1;
+            if (has_s) mma_commit(bar(kBarSFull + t));
+            if (has_pv) {
+              if (j - 1 == nt - 1) mma_commit(bar(kBarOFull + t));
+              mma_commit(bar(kBarEmpty + sV));  // this tile's last use of V_{j-1}
+            }
+            if (has_s) {
+              mma_commit(bar(kBarEmpty + sK));  // this tile's use of K_j
+              if (j == nt - 1) mma_commit(bar(kBarQEmpty));  // this tile's last read of Q
+            }
+            if (unused) {  // K_j and V_j are not visible to this tile
+              mma_commit(bar(kBarEmpty + sK));
+              mma_commit(bar(kBarEmpty + sV2));
             }
           }
-          if (has_s) {
-            // S_t = Q_t K_j^T
-            const uint64_t qd = sw128_desc(qt, 16, 1024), kd = sw128_desc(k_base, 16, 1024);
+          c += 2 * n_max;
+          g += nt;
+          base += 2 * (n_max + 1);
+        }
+      } else {
+        int cur_blk = 0;  // block of the previous item (block tables)
+        for (long long i = 0, k = item_index(0); k < n_items && ok; k = item_index(++i)) {
+          const Item it = item_of(p, tbl, k, cur_blk);
+          bool any = false;
+          int last_sg = -1;  // this tile's last segment with a KV tile: its last S reads Q
+          for (int sg = 0; sg < n_segs; ++sg) {
+            any |= seg_max(it, sg) > 0;
+            if (tiles(it, sg, t) > 0) last_sg = sg;
+          }
+          if (!any) continue;
+          if (!mbar_wait(bar(kBarQFull), nq & 1, abort_flag, err)) break;
+          ++nq;
+          if (last_sg < 0) mma_commit(bar(kBarQEmpty));  // this tile reads nothing of Q
+          for (int sg = 0; sg < n_segs && ok; ++sg) {  // the segments in turn, Q staying
+            const int nt = tiles(it, sg, t);
+            const int n_max = seg_max(it, sg);
+            if (n_max == 0) continue;
+            // Burst slots alternate between the tiles: (step j, tile t) is slot
+            // base + 2 j + t. A tile waits for its data before its slot comes up
+            // and makes its commits after handing the slot on, so that its
+            // waits and commits overlap the other tile's MMAs.
+            for (int j = 0; ok && j <= n_max; ++j) {
+              const int cK = c + 2 * j, cV = c + 2 * j - 1;  // ring positions of K_j and V_{j-1}
+              const int sK = cK % C::kStages, sV = (cV + C::kStages) % C::kStages;
+              const int cV2 = cK + 1, sV2 = cV2 % C::kStages;  // V_j
+              const uint32_t k_base = ring_base + sK * C::kTileBytes;
+              const uint32_t v_base = ring_base + sV * C::kTileBytes;
+              const bool has_pv = j >= 1 && j - 1 < nt, has_s = j < nt, unused = !has_s && j < n_max;
+              // the data first (usually there already), the softmax's P last
+              if ((has_s || unused) && !mbar_wait(bar(kBarFull + sK), (cK / C::kStages) & 1, abort_flag, err)) {
+                ok = false;
+                break;
+              }
+              if (unused && !mbar_wait(bar(kBarFull + sV2), (cV2 / C::kStages) & 1, abort_flag, err)) {
+                ok = false;
+                break;
+              }
+              if (has_pv && (!mbar_wait(bar(kBarFull + sV), (cV / C::kStages) & 1, abort_flag, err) ||
+                             !mbar_wait(bar(kBarPFull + t), (g + j - 1) & 1, abort_flag, err))) {
+                ok = false;
+                break;
+              }
+              const int slot = base + 2 * j + t;
+              if (!wait_turn(turn, slot, abort_flag, err)) {
+                ok = false;
+                break;
+              }
+              if (has_pv) {
+                // O_t += P_t V_{j-1}; P_t was written over S_t by the softmax
+                // warps. For j = 1 this overwrites O_t: the warpgroup read the
+                // previous segment's O_t before it signalled this P.
+                tc_fence_after();
+                if constexpr (kFp8) {
 #pragma unroll
-            for (int kk = 0; kk < kKSteps; ++kk) {
-              const uint64_t off = static_cast<uint64_t>(((kk / 4) * kColBlockBytes + (kk % 4) * 32) >> 4);
-              if constexpr (kFp8)
-                mma_ss_e4m3(s_col, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
-              else
-                mma_ss(s_col, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+                  for (int kk = 0; kk < kRowsPerTile / 32; ++kk)
+                    mma_ts_e4m3(o_col, s_col + kk * 8, sw128_desc(v_base + kk * 32, 16, 1024), idesc_o,
+                                (j > 1 || kk > 0) ? 1u : 0u);
+                } else {
+                  // descriptor start fields advance by 2048 / 16 per 16 keys
+                  const uint64_t vd = sw128_desc(v_base, kColBlockBytes, 1024);
+                  mma_ts(o_col, s_col, vd, idesc_o, j > 1 ? 1u : 0u);
+#pragma unroll
+                  for (int kk = 1; kk < kRowsPerTile / 16; ++kk)
+                    mma_ts(o_col, s_col + kk * 8, vd + static_cast<uint64_t>(kk * 128), idesc_o, 1u);
+                }
+              }
+              if (has_s) {
+                // S_t = Q_t K_j^T
+                const uint64_t qd = sw128_desc(qt, 16, 1024), kd = sw128_desc(k_base, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < kKSteps; ++kk) {
+                  const uint64_t off = static_cast<uint64_t>(((kk / 4) * kColBlockBytes + (kk % 4) * 32) >> 4);
+                  if constexpr (kFp8)
+                    mma_ss_e4m3(s_col, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+                  else
+                    mma_ss(s_col, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+                }
+              }
+              *turn = slot + 1;
+              if (has_s) mma_commit(bar(kBarSFull + t));
+              if (has_pv) {
+                if (j - 1 == nt - 1) mma_commit(bar(kBarOFull + t));
+                mma_commit(bar(kBarEmpty + sV));  // this tile's last use of V_{j-1}
+              }
+              if (has_s) {
+                mma_commit(bar(kBarEmpty + sK));  // this tile's use of K_j
+                if (j == nt - 1 && sg == last_sg) mma_commit(bar(kBarQEmpty));  // its last read of Q
+              }
+              if (unused) {  // K_j and V_j are not visible to this tile
+                mma_commit(bar(kBarEmpty + sK));
+                mma_commit(bar(kBarEmpty + sV2));
+              }
             }
-          }
-          *turn = slot + 1;
-          if (has_s) mma_commit(bar(kBarSFull + t));
-          if (has_pv) {
-            if (j - 1 == nt - 1) mma_commit(bar(kBarOFull + t));
-            mma_commit(bar(kBarEmpty + sV));  // this tile's last use of V_{j-1}
-          }
-          if (has_s) {
-            mma_commit(bar(kBarEmpty + sK));  // this tile's use of K_j
-            if (j == nt - 1) mma_commit(bar(kBarQEmpty));  // this tile's last read of Q
-          }
-          if (unused) {  // K_j and V_j are not visible to this tile
-            mma_commit(bar(kBarEmpty + sK));
-            mma_commit(bar(kBarEmpty + sV2));
+            c += 2 * n_max;
+            g += nt;
+            base += 2 * (n_max + 1);
           }
         }
-        c += 2 * n_max;
-        g += nt;
-        base += 2 * (n_max + 1);
       }
       // All MMAs issued here must be complete before TMEM is released.
       mma_commit(bar(kBarMmaDone));
@@ -411,34 +589,69 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t pfull = bar(kBarPFull + t);
     const uint32_t stage = smem_addr(sStage + t * C::kStageBytes);
-    int g = 0;       // KV steps of this tile over earlier items
-    uint32_t u = 0;  // earlier items in which this tile visited a KV tile
-    int cur_blk = 0;  // block of the previous item (block tables)
-    for (long long i = 0, k = item_index(0); k < n_items; k = item_index(++i)) {
-      const Item it = item_of(p, tbl, k, cur_blk);
-      const BlockDesc blk = block_of(p, tbl, it.blk);
-      const int out_head = blk.part * p.B * p.Hq + it.bh;  // head of O / lse written
-      const int tile_first = it.row0 + t * kRowsPerTile;
-      const int n = tiles(it, t);
-      if (n == 0) {
-        write_empty_rows<D, kF32Out>(p, blk, out_head, tile_first, kRowsPerTile,
-                                     threadIdx.x & 127, 128);
-        continue;
+    if constexpr (!kSeg) {
+      int g = 0;       // KV steps of this tile over earlier items
+      uint32_t u = 0;  // earlier items in which this tile visited a KV tile
+      int cur_blk = 0;  // block of the previous item (block tables)
+      for (long long i = 0, k = item_index(0); k < n_items; k = item_index(++i)) {
+        const Item it = item_of(p, tbl, k, cur_blk);
+        const BlockDesc blk = block_of(p, tbl, it.blk);
+        const int out_head = blk.part * p.B * p.Hq + it.bh;  // head of O / lse written
+        const int tile_first = it.row0 + t * kRowsPerTile;
+        const int n = tiles(it, 0, t);
+        if (n == 0) {
+          write_empty_rows<D, kF32Out>(p, blk, out_head, tile_first, kRowsPerTile,
+                                       threadIdx.x & 127, 128);
+          continue;
+        }
+        const int row = tile_first + row_in_tile;
+        const EpilogueStore store{&tm_o, stage, 1 + t, out_head};
+        auto signal_p = [&] {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(pfull);  // one arrival per warp
+        };
+        const bool ok = softmax_row<D, kF32Out, decltype(signal_p), kFp8>(
+            p, blk, row, tile_first, n, tS(t) + lane_off, tO(t) + lane_off, bar(kBarSFull + t),
+            bar(kBarOFull + t), g, u & 1u,
+            static_cast<size_t>(out_head) * p.o_rows + static_cast<size_t>(blk.o_row + row),
+            abort_flag, err, store, signal_p);
+        g += n;
+        ++u;
+        if (!ok) break;  // the same on every thread of the warpgroup
       }
-      const int row = tile_first + row_in_tile;
-      const EpilogueStore store{&tm_o, stage, 1 + t, out_head};
-      auto signal_p = [&] {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(pfull);  // one arrival per warp
-      };
-      const bool ok = softmax_row<D, kF32Out, decltype(signal_p), kFp8>(
-          p, blk, row, tile_first, n, tS(t) + lane_off, tO(t) + lane_off, bar(kBarSFull + t),
-          bar(kBarOFull + t), g, u & 1u,
-          static_cast<size_t>(out_head) * p.o_rows + static_cast<size_t>(blk.o_row + row),
-          abort_flag, err, store, signal_p);
-      g += n;
-      ++u;
-      if (!ok) break;  // the same on every thread of the warpgroup
+    } else {
+      int g = 0;       // KV steps of this tile over earlier segments
+      uint32_t u = 0;  // earlier segments in which this tile visited a KV tile
+      int cur_blk = 0;  // block of the previous item (block tables)
+      bool ok = true;
+      for (long long i = 0, k = item_index(0); k < n_items && ok; k = item_index(++i)) {
+        const Item it = item_of(p, tbl, k, cur_blk);
+        for (int sg = 0; sg < n_segs && ok; ++sg) {  // each segment's partial in turn
+          const BlockDesc blk = seg_block(p, tbl, it, sg);
+          const int out_head = blk.part * p.B * p.Hq + it.bh;  // head of O / lse written
+          const int tile_first = it.row0 + t * kRowsPerTile;
+          const int n = tiles(it, sg, t);
+          if (n == 0) {
+            write_empty_rows<D, kF32Out>(p, blk, out_head, tile_first, kRowsPerTile,
+                                         threadIdx.x & 127, 128);
+            continue;
+          }
+          const int row = tile_first + row_in_tile;
+          const EpilogueStore store{&tm_o, stage, 1 + t, out_head};
+          auto signal_p = [&] {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pfull);  // one arrival per warp
+          };
+          // a failed segment ends both loops, the same on every thread of the warpgroup
+          ok = softmax_row<D, kF32Out, decltype(signal_p), kFp8>(
+              p, blk, row, tile_first, n, tS(t) + lane_off, tO(t) + lane_off, bar(kBarSFull + t),
+              bar(kBarOFull + t), g, u & 1u,
+              static_cast<size_t>(out_head) * p.o_rows + static_cast<size_t>(blk.o_row + row),
+              abort_flag, err, store, signal_p);
+          g += n;
+          ++u;
+        }
+      }
     }
     // the epilogue's last TMA stores (issued by lane 0 of each warp): read out
     // of shared memory and written to global memory before the CTA's shared
@@ -521,6 +734,14 @@ cudaError_t launch_attention_blocks(int D, bool f32_out, const CUtensorMap &tq,
                                     const CUtensorMap &to, const AttnParams &p,
                                     const BlockTable &tbl, cudaStream_t stream) {
   return launch_dispatch(D, f32_out, tq, tk, tv, to, p, tbl, tbl.item_start[tbl.n], stream);
+}
+
+cudaError_t launch_attention_segments(int D, bool f32_out, const CUtensorMap &tq,
+                                      const CUtensorMap &tk, const CUtensorMap &tv,
+                                      const CUtensorMap &to, const AttnParams &p,
+                                      const SegTable &tbl, cudaStream_t stream) {
+  const long long items = static_cast<long long>(p.B) * p.Hq * ((tbl.b[0].Sq + 255) / 256);
+  return launch_dispatch(D, f32_out, tq, tk, tv, to, p, tbl, items, stream);
 }
 
 namespace {

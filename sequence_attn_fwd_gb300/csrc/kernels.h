@@ -45,6 +45,15 @@ struct BlockTable {
   BlockDesc b[kMaxLaunchBlocks];
 };
 
+// Blocks that share their query rows (q_row, o_row, q_pos and Sq equal to
+// block 0's), such as the key chunks of a ring pass: a work item is 256 of
+// those rows of one (batch, head) taken against every block in turn, each
+// block a segment of the item with its own partial, Q loaded once.
+struct SegTable {
+  int n;
+  BlockDesc b[kMaxLaunchBlocks];
+};
+
 // Tensor maps are 3-D views [heads][rows][D] built by the caller: q, k, v of
 // bf16 data, box 64 columns x 128 rows x 1; o of the output type (fp32 when
 // f32_out, else bf16), box 128 bytes x 32 rows x 1 (one warp's rows); all with
@@ -84,6 +93,13 @@ cudaError_t launch_attention_blocks(int D, bool f32_out, const CUtensorMap &tm_q
                                     const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                                     const CUtensorMap &tm_o, const AttnParams &p,
                                     const BlockTable &tbl, cudaStream_t stream);
+
+// The same kernel over a table of blocks that share their query rows (see
+// SegTable; p's Sq / Skv / q_off / kv_off / n_qblocks are unused).
+cudaError_t launch_attention_segments(int D, bool f32_out, const CUtensorMap &tm_q,
+                                      const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                                      const CUtensorMap &tm_o, const AttnParams &p,
+                                      const SegTable &tbl, cudaStream_t stream);
 
 cudaError_t launch_lse_merge(const float *o_parts, const float *lse_parts, int P, long long nrows,
                              int D, void *o, bool bf16_out, float *lse, cudaStream_t stream);

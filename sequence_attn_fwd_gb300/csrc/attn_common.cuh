@@ -89,26 +89,16 @@ __device__ __forceinline__ uint64_t exp2_poly_x2(uint64_t x) {
                  __uint_as_float(__float_as_uint(p1) + (__float_as_uint(t1) << 23)));
 }
 
-// Of every 8 pairs of a row's exponentials, this many take exp2_poly_x2 and
-// the rest the MUFU ex2 (GB300's MUFU does 32 ex2 per clock per SM, so the
-// softmax is bound by instruction issue rather than by the MUFU): none for
-// bf16 output and for e4m3 inputs, where every polynomial adds issue slots;
-// two for the fp32 partials, whose kernel measured faster with them (short
-// key chunks, where the fp32 epilogue's registers compete with the row's).
-#ifndef SEQATTN_POLY_EXP_PAIRS_PER_8_F32OUT
-#define SEQATTN_POLY_EXP_PAIRS_PER_8_F32OUT 2
-#endif
-#ifndef SEQATTN_POLY_EXP_PAIRS_PER_8_BF16OUT
-#define SEQATTN_POLY_EXP_PAIRS_PER_8_BF16OUT 0
-#endif
-#ifndef SEQATTN_POLY_EXP_PAIRS_PER_8_FP8
-#define SEQATTN_POLY_EXP_PAIRS_PER_8_FP8 0
-#endif
-template <bool kF32Out, bool kFp8>
-constexpr int poly_pairs_per_8() {
-  return kFp8 ? SEQATTN_POLY_EXP_PAIRS_PER_8_FP8
-              : (kF32Out ? SEQATTN_POLY_EXP_PAIRS_PER_8_F32OUT : SEQATTN_POLY_EXP_PAIRS_PER_8_BF16OUT);
-}
+// Of every 8 pairs of a row's exponentials, the kernel's kPoly take
+// exp2_poly_x2 and the rest the MUFU ex2 (GB300's MUFU does 32 ex2 per clock
+// per SM, so the softmax is bound by instruction issue rather than by the
+// MUFU). The launch picks none for bf16 output, for e4m3 inputs and for fp32
+// partials of blocks longer than kPolyMaxKeys, where every polynomial adds
+// issue slots, and kPolyPairsShort for fp32 partials of short blocks, whose
+// kernel measured faster with them (short items, where the fp32 epilogue's
+// registers compete with the row's).
+constexpr int kPolyPairsShort = 2;
+constexpr int kPolyMaxKeys = 2048;
 
 __device__ __forceinline__ uint64_t exp2_pair(uint64_t x, bool poly) {
   if (poly) return exp2_poly_x2(x);
@@ -194,7 +184,7 @@ struct EpilogueStore {
 //                     that works through several tiles keeps counting)
 //   ofull_parity      parity of the bar_ofull phase that marks this tile's O
 // Returns false if the pipeline was aborted.
-template <int D, bool kF32Out, typename SignalP, bool kFp8 = false>
+template <int D, bool kF32Out, typename SignalP, bool kFp8, int kPoly>
 __device__ __forceinline__ bool softmax_row(const AttnParams &p, const BlockDesc &blk, int row,
                                             int tile_first_row, int n,
                                             uint32_t s_addr, uint32_t o_addr, uint32_t bar_sfull,
@@ -205,7 +195,6 @@ __device__ __forceinline__ bool softmax_row(const AttnParams &p, const BlockDesc
     const long long qpos = blk.q_pos + row;
     const long long tile_first_q = blk.q_pos + tile_first_row;
     const float c2 = p.scale_log2;
-    constexpr int kPoly = poly_pairs_per_8<kF32Out, kFp8>();
     float m = -INFINITY;  // running max of scale*log2(e)*s (the reference for P)
     float l = 0.f;        // running sum of P relative to m
     bool ok = true;

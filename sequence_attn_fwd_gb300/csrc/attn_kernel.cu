@@ -184,7 +184,7 @@ __device__ __forceinline__ BlockDesc seg_block(const AttnParams &, const SegTabl
 // kFp8: Q, K in e4m3 with K-major tiles, V given transposed ([heads][D][keys],
 // so its tiles are K-major too), P rounded to e4m3 in TMEM (one instantiation:
 // D = 128, bf16 output, single problem).
-template <int D, bool kF32Out, typename Table, bool kFp8>
+template <int D, bool kF32Out, typename Table, bool kFp8, int kPoly>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -610,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(pfull);  // one arrival per warp
         };
-        const bool ok = softmax_row<D, kF32Out, decltype(signal_p), kFp8>(
+        const bool ok = softmax_row<D, kF32Out, decltype(signal_p), kFp8, kPoly>(
             p, blk, row, tile_first, n, tS(t) + lane_off, tO(t) + lane_off, bar(kBarSFull + t),
             bar(kBarOFull + t), g, u & 1u,
             static_cast<size_t>(out_head) * p.o_rows + static_cast<size_t>(blk.o_row + row),
@@ -643,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(pfull);  // one arrival per warp
           };
           // a failed segment ends both loops, the same on every thread of the warpgroup
-          ok = softmax_row<D, kF32Out, decltype(signal_p), kFp8>(
+          ok = softmax_row<D, kF32Out, decltype(signal_p), kFp8, kPoly>(
               p, blk, row, tile_first, n, tS(t) + lane_off, tO(t) + lane_off, bar(kBarSFull + t),
               bar(kBarOFull + t), g, u & 1u,
               static_cast<size_t>(out_head) * p.o_rows + static_cast<size_t>(blk.o_row + row),
@@ -683,11 +683,11 @@ int sm_count() {
   return n;
 }
 
-template <int D, bool kF32Out, typename Table, bool kFp8 = false>
+template <int D, bool kF32Out, typename Table, bool kFp8, int kPoly>
 cudaError_t launch_typed(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                          const CUtensorMap &to, const AttnParams &p, const Table &tbl,
                          long long n_items, cudaStream_t stream) {
-  auto kernel = attn_fwd_kernel<D, kF32Out, Table, kFp8>;
+  auto kernel = attn_fwd_kernel<D, kF32Out, Table, kFp8, kPoly>;
   constexpr int kSmem = Cfg<D, kFp8>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
@@ -698,14 +698,27 @@ cudaError_t launch_typed(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
   return cudaGetLastError();
 }
 
+// bf16 output: every exponential on the MUFU. fp32 partials: kPolyPairsShort
+// of every 8 pairs on the FMA pipe, unless some block is longer than
+// kPolyMaxKeys (segment tables hold short blocks only).
+template <int D, typename Table>
+cudaError_t launch_out(bool f32_out, bool long_keys, const CUtensorMap &tq, const CUtensorMap &tk,
+                       const CUtensorMap &tv, const CUtensorMap &to, const AttnParams &p,
+                       const Table &tbl, long long n_items, cudaStream_t stream) {
+  if (!f32_out) return launch_typed<D, false, Table, false, 0>(tq, tk, tv, to, p, tbl, n_items, stream);
+  if constexpr (!std::is_same<Table, SegTable>::value) {
+    if (long_keys) return launch_typed<D, true, Table, false, 0>(tq, tk, tv, to, p, tbl, n_items, stream);
+  }
+  return launch_typed<D, true, Table, false, kPolyPairsShort>(tq, tk, tv, to, p, tbl, n_items, stream);
+}
+
 template <typename Table>
-cudaError_t launch_dispatch(int D, bool f32_out, const CUtensorMap &tq, const CUtensorMap &tk,
-                            const CUtensorMap &tv, const CUtensorMap &to, const AttnParams &p,
-                            const Table &tbl, long long n_items, cudaStream_t stream) {
-  if (D == 128) return f32_out ? launch_typed<128, true>(tq, tk, tv, to, p, tbl, n_items, stream)
-                               : launch_typed<128, false>(tq, tk, tv, to, p, tbl, n_items, stream);
-  return f32_out ? launch_typed<64, true>(tq, tk, tv, to, p, tbl, n_items, stream)
-                 : launch_typed<64, false>(tq, tk, tv, to, p, tbl, n_items, stream);
+cudaError_t launch_dispatch(int D, bool f32_out, bool long_keys, const CUtensorMap &tq,
+                            const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &to,
+                            const AttnParams &p, const Table &tbl, long long n_items,
+                            cudaStream_t stream) {
+  if (D == 128) return launch_out<128>(f32_out, long_keys, tq, tk, tv, to, p, tbl, n_items, stream);
+  return launch_out<64>(f32_out, long_keys, tq, tk, tv, to, p, tbl, n_items, stream);
 }
 
 }  // namespace
@@ -718,14 +731,14 @@ namespace seqattn {
 cudaError_t launch_attention(int D, bool f32_out, const CUtensorMap &tq, const CUtensorMap &tk,
                              const CUtensorMap &tv, const CUtensorMap &to, const AttnParams &p,
                              cudaStream_t stream) {
-  return launch_dispatch(D, f32_out, tq, tk, tv, to, p, SingleProblem{0},
+  return launch_dispatch(D, f32_out, p.Skv > kPolyMaxKeys, tq, tk, tv, to, p, SingleProblem{0},
                          static_cast<long long>(p.B) * p.Hq * p.n_qblocks, stream);
 }
 
 cudaError_t launch_attention_fp8(const CUtensorMap &tq, const CUtensorMap &tk,
                                  const CUtensorMap &tvt, const CUtensorMap &to,
                                  const AttnParams &p, cudaStream_t stream) {
-  return launch_typed<128, false, SingleProblem, true>(
+  return launch_typed<128, false, SingleProblem, true, 0>(
       tq, tk, tvt, to, p, SingleProblem{0}, static_cast<long long>(p.B) * p.Hq * p.n_qblocks, stream);
 }
 
@@ -733,7 +746,9 @@ cudaError_t launch_attention_blocks(int D, bool f32_out, const CUtensorMap &tq,
                                     const CUtensorMap &tk, const CUtensorMap &tv,
                                     const CUtensorMap &to, const AttnParams &p,
                                     const BlockTable &tbl, cudaStream_t stream) {
-  return launch_dispatch(D, f32_out, tq, tk, tv, to, p, tbl, tbl.item_start[tbl.n], stream);
+  bool long_keys = false;
+  for (int i = 0; i < tbl.n; ++i) long_keys = long_keys || tbl.b[i].Skv > kPolyMaxKeys;
+  return launch_dispatch(D, f32_out, long_keys, tq, tk, tv, to, p, tbl, tbl.item_start[tbl.n], stream);
 }
 
 cudaError_t launch_attention_segments(int D, bool f32_out, const CUtensorMap &tq,
@@ -741,7 +756,7 @@ cudaError_t launch_attention_segments(int D, bool f32_out, const CUtensorMap &tq
                                       const CUtensorMap &to, const AttnParams &p,
                                       const SegTable &tbl, cudaStream_t stream) {
   const long long items = static_cast<long long>(p.B) * p.Hq * ((tbl.b[0].Sq + 255) / 256);
-  return launch_dispatch(D, f32_out, tq, tk, tv, to, p, tbl, items, stream);
+  return launch_dispatch(D, f32_out, false, tq, tk, tv, to, p, tbl, items, stream);
 }
 
 namespace {

@@ -127,6 +127,30 @@ def test_attn_partial_offsets_against_oracle(sa, q_off, a, b):
     check_lse(lse, lse_ref)
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_attn_partial_long_blocks_against_oracle(sa, D):
+    """fp32 partials of blocks longer than 2048 keys take every exponential on
+    the MUFU (shorter ones put a share on the FMA-pipe polynomial): a 2500-key
+    chunk as a single problem, and as one block of a table beside a short one,
+    checked in full against the oracle."""
+    B, Hq, Hkv, S = 1, 4, 2, 2900
+    a = 400  # the long chunk is keys [400, 2900): 2500 keys
+    q, k, v = workloads.make_qkv(adhoc(B, Hq, Hkv, S, D, True, seed=17))
+    qd, kd, vd = to_dev(q, k, v)
+    o_ref, lse_ref = oracle.attention(q, k[:, :, a:].contiguous(), v[:, :, a:].contiguous(), True, kv_off=a)
+    o, lse = sa.attn_partial(qd, kd[:, :, a:], vd[:, :, a:], 0, a, True)
+    check_o(o, o_ref, bf16_out=False)
+    check_lse(lse, lse_ref)
+    # the same chunk in a block table with the short chunk [0, 400) beside it (part 1)
+    o2, l2 = sa.attn_partial_blocks(qd, kd, vd, [(0, a, 0, 0, a, S, S - a, 0), (0, 0, 0, 0, 0, S, a, 1)],
+                                    n_parts=2, causal=True)
+    check_o(o2[0], o_ref, bf16_out=False)
+    check_lse(l2[0], lse_ref)
+    o_ref1, lse_ref1 = oracle.attention(q, k[:, :, :a].contiguous(), v[:, :, :a].contiguous(), True)
+    check_o(o2[1], o_ref1, bf16_out=False)
+    check_lse(l2[1], lse_ref1)
+
+
 def test_attn_partial_chunk_invisible_to_every_row(sa):
     q, k, v = to_dev(*workloads.make_qkv(adhoc(1, 2, 2, 512, 64, True)))
     o, lse = sa.attn_partial(q[:, :, :256].contiguous(), k[:, :, 256:], v[:, :, 256:], 0, 256, True)

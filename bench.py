@@ -100,14 +100,17 @@ def merge_algorithmic_bytes(w: workloads.Workload, out_bytes: int = 2) -> int:
     return w.P * rows * 4 + finite_rows * w.D * 4 + rows * w.D * out_bytes + rows * 4
 
 
+# The kernels' sources and the C-ABI layer that sets up their launches (the
+# tables, item order and grid decide the traffic as much as the kernel code).
+_FWD_SOURCES = ["attn_kernel.cu", "attn_common.cuh", "ptx.cuh", "kernels.h", "api.cu"]
 KERNEL_SOURCES = {
-    "attn_bwd": ["attn_kernel.cu", "attn_bwd.cuh", "ptx.cuh"],
-    "attn_partial": ["attn_kernel.cu", "attn_common.cuh", "ptx.cuh"],
-    "attn_partial_blocks": ["attn_kernel.cu", "attn_common.cuh", "ptx.cuh"],
-    "attn_fwd_varlen": ["attn_kernel.cu", "attn_common.cuh", "ptx.cuh"],
-    "attn_fwd_fp8": ["attn_kernel.cu", "attn_common.cuh", "ptx.cuh"],
-    "attn_fwd": ["attn_kernel.cu", "attn_common.cuh", "ptx.cuh"],
-    "lse_merge": ["lse_merge.cu"],
+    "attn_bwd": ["attn_kernel.cu", "attn_bwd.cuh", "ptx.cuh", "kernels.h", "api.cu"],
+    "attn_partial": _FWD_SOURCES,
+    "attn_partial_blocks": _FWD_SOURCES,
+    "attn_fwd_varlen": _FWD_SOURCES,
+    "attn_fwd_fp8": _FWD_SOURCES,
+    "attn_fwd": _FWD_SOURCES,
+    "lse_merge": ["lse_merge.cu", "kernels.h", "api.cu"],
 }
 
 

@@ -198,9 +198,12 @@ int run_blocks(const void *q, const void *k, const void *v, void *o, float *lse,
   // previous chunk's last product, which pays where an item's fixed cost is a
   // large part of its work. Longer chunks keep the block table, whose items
   // run one chunk after another and so keep a chunk's K and V in L2, where
-  // segments would stream the K and V of every chunk at once.
+  // segments would stream the K and V of every chunk at once; so do lists
+  // whose shared rows make fewer items than the GPU has SMs, where one item a
+  // block keeps more SMs busy.
   constexpr int kSegMaxKeys = 2048;
-  bool shared_q = blocks.size() >= 2 && blocks[0].Sq > 0;
+  bool shared_q = blocks.size() >= 2 && blocks[0].Sq > 0 &&
+                  heads * ((blocks[0].Sq + 255) / 256) >= seqattn::device_sm_count();
   for (const auto &b : blocks)
     shared_q = shared_q && b.q_row == blocks[0].q_row && b.o_row == blocks[0].o_row &&
                b.q_pos == blocks[0].q_pos && b.Sq == blocks[0].Sq && b.Skv <= kSegMaxKeys;

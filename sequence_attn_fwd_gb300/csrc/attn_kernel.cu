@@ -728,6 +728,8 @@ cudaError_t launch_dispatch(int D, bool f32_out, bool long_keys, const CUtensorM
 
 namespace seqattn {
 
+int device_sm_count() { return sm_count(); }
+
 cudaError_t launch_attention(int D, bool f32_out, const CUtensorMap &tq, const CUtensorMap &tk,
                              const CUtensorMap &tv, const CUtensorMap &to, const AttnParams &p,
                              cudaStream_t stream) {

@@ -54,6 +54,9 @@ struct SegTable {
   BlockDesc b[kMaxLaunchBlocks];
 };
 
+// Number of SMs of the current device (read once per device).
+int device_sm_count();
+
 // Tensor maps are 3-D views [heads][rows][D] built by the caller: q, k, v of
 // bf16 data, box 64 columns x 128 rows x 1; o of the output type (fp32 when
 // f32_out, else bf16), box 128 bytes x 32 rows x 1 (one warp's rows); all with

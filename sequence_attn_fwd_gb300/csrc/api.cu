@@ -202,7 +202,7 @@ int run_blocks(const void *q, const void *k, const void *v, void *o, float *lse,
   // whose shared rows make fewer items than the GPU has SMs, where one item a
   // block keeps more SMs busy.
   constexpr int kSegMaxKeys = 2048;
-  bool shared_q = blocks.size() >= 2 && blocks[0].Sq > 0 &&
+  bool shared_q = f32_out && blocks.size() >= 2 && blocks[0].Sq > 0 &&
                   heads * ((blocks[0].Sq + 255) / 256) >= seqattn::device_sm_count();
   for (const auto &b : blocks)
     shared_q = shared_q && b.q_row == blocks[0].q_row && b.o_row == blocks[0].o_row &&

@@ -700,13 +700,16 @@ cudaError_t launch_typed(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
 
 // bf16 output: every exponential on the MUFU. fp32 partials: kPolyPairsShort
 // of every 8 pairs on the FMA pipe, unless some block is longer than
-// kPolyMaxKeys (segment tables hold short blocks only).
+// kPolyMaxKeys. Segment tables (the partials of short blocks) come with fp32
+// output only.
 template <int D, typename Table>
 cudaError_t launch_out(bool f32_out, bool long_keys, const CUtensorMap &tq, const CUtensorMap &tk,
                        const CUtensorMap &tv, const CUtensorMap &to, const AttnParams &p,
                        const Table &tbl, long long n_items, cudaStream_t stream) {
-  if (!f32_out) return launch_typed<D, false, Table, false, 0>(tq, tk, tv, to, p, tbl, n_items, stream);
-  if constexpr (!std::is_same<Table, SegTable>::value) {
+  if constexpr (std::is_same<Table, SegTable>::value) {
+    if (!f32_out || long_keys) return cudaErrorInvalidValue;
+  } else {
+    if (!f32_out) return launch_typed<D, false, Table, false, 0>(tq, tk, tv, to, p, tbl, n_items, stream);
     if (long_keys) return launch_typed<D, true, Table, false, 0>(tq, tk, tv, to, p, tbl, n_items, stream);
   }
   return launch_typed<D, true, Table, false, kPolyPairsShort>(tq, tk, tv, to, p, tbl, n_items, stream);
@@ -757,8 +760,10 @@ cudaError_t launch_attention_segments(int D, bool f32_out, const CUtensorMap &tq
                                       const CUtensorMap &tk, const CUtensorMap &tv,
                                       const CUtensorMap &to, const AttnParams &p,
                                       const SegTable &tbl, cudaStream_t stream) {
+  bool long_keys = false;
+  for (int i = 0; i < tbl.n; ++i) long_keys = long_keys || tbl.b[i].Skv > kPolyMaxKeys;
   const long long items = static_cast<long long>(p.B) * p.Hq * ((tbl.b[0].Sq + 255) / 256);
-  return launch_dispatch(D, f32_out, false, tq, tk, tv, to, p, tbl, items, stream);
+  return launch_dispatch(D, f32_out, long_keys, tq, tk, tv, to, p, tbl, items, stream);
 }
 
 namespace {

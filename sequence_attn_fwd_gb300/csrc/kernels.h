@@ -98,7 +98,9 @@ cudaError_t launch_attention_blocks(int D, bool f32_out, const CUtensorMap &tm_q
                                     const BlockTable &tbl, cudaStream_t stream);
 
 // The same kernel over a table of blocks that share their query rows (see
-// SegTable; p's Sq / Skv / q_off / kv_off / n_qblocks are unused).
+// SegTable; p's Sq / Skv / q_off / kv_off / n_qblocks are unused): fp32
+// partials of blocks of at most 2048 keys (anything else is refused with
+// cudaErrorInvalidValue).
 cudaError_t launch_attention_segments(int D, bool f32_out, const CUtensorMap &tm_q,
                                       const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                                       const CUtensorMap &tm_o, const AttnParams &p,

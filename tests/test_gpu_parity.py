@@ -358,38 +358,44 @@ def test_single_problem_head_chunks_cover_every_row(sa, D, Hq, Hkv):
     check_lse(gather_rows(l1, rows), lse_ref)
 
 
-@pytest.mark.parametrize("D,Hq,Hkv,S,P", [(128, 8, 4, 16384, 8), (64, 6, 2, 13200, 66)],
-                         ids=["d128_8x2048", "d64_66x200"])
-def test_shared_query_segments_match_block_table(sa, D, Hq, Hkv, S, P):
+@pytest.mark.parametrize("D,Hq,Hkv,S,P,causal,skip_empty",
+                         [(128, 8, 4, 16384, 8, True, False), (64, 6, 2, 13200, 66, True, False),
+                          (128, 8, 4, 16384, 8, True, True), (128, 8, 4, 8192, 4, False, False)],
+                         ids=["d128_8x2048", "d64_66x200", "d128_8x2048_skip", "d128_4x2048_noncausal"])
+def test_shared_query_segments_match_block_table(sa, D, Hq, Hkv, S, P, causal, skip_empty):
     """Short key chunks that share all their query rows (one ring pass's
     blocks of a query chunk) run as the segments of each work item, Q loaded
-    once (here 8 chunks of 2048 keys, and 66 ragged chunks of 200 keys, split
+    once (here chunks of 2048 keys, and 66 ragged chunks of 200 keys, split
     into launches of 64 and 2 segments). Each chunk's fp32 partial and lse must
     be bitwise those of the same block launched alone (the block-table
-    kernel); all outputs start as NaN, so a row that no segment wrote fails. A
-    few rows of the first and last chunks are also checked against the
-    oracle."""
+    kernel); all outputs start as NaN (as 7.0 with skip_empty, whose rows
+    before a chunk's first key keep that value), so a row that no segment
+    wrote fails. A few rows of the first and last chunks are also checked
+    against the oracle."""
     C = S // P
-    w = adhoc(1, Hq, Hkv, S, D, True, seed=93)
+    w = adhoc(1, Hq, Hkv, S, D, causal, seed=93)
     q, k, v = workloads.make_qkv(w)
     qd, kd, vd = to_dev(q, k, v)
-    nan = float("nan")
+    fill = 7.0 if skip_empty else float("nan")
     blocks = [(0, j * C, 0, 0, j * C, S, C, j) for j in range(P)]
-    o1 = torch.full((P, 1, Hq, S, D), nan, device="cuda")
-    l1 = torch.full((P, 1, Hq, S), nan, device="cuda")
-    sa.attn_partial_blocks(qd, kd, vd, blocks, n_parts=P, causal=True, out=o1, lse=l1)
-    o2 = torch.full((P, 1, Hq, S, D), nan, device="cuda")
-    l2 = torch.full((P, 1, Hq, S), nan, device="cuda")
+    o1 = torch.full((P, 1, Hq, S, D), fill, device="cuda")
+    l1 = torch.full((P, 1, Hq, S), fill, device="cuda")
+    sa.attn_partial_blocks(qd, kd, vd, blocks, n_parts=P, causal=causal, out=o1, lse=l1, skip_empty=skip_empty)
+    o2 = torch.full((P, 1, Hq, S, D), fill, device="cuda")
+    l2 = torch.full((P, 1, Hq, S), fill, device="cuda")
     for b in blocks:
-        sa.attn_partial_blocks(qd, kd, vd, [b], n_parts=P, causal=True, out=o2, lse=l2)
+        sa.attn_partial_blocks(qd, kd, vd, [b], n_parts=P, causal=causal, out=o2, lse=l2, skip_empty=skip_empty)
     torch.cuda.synchronize()
     sa.query_device_error()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    if skip_empty:  # rows before each chunk's first key: O untouched, lse -inf
+        for j in range(1, P):
+            assert (o1[j, :, :, :j * C] == fill).all() and torch.isneginf(l1[j, :, :, :j * C]).all()
     del o2, l2
     rows = workloads.sample_query_rows(w, n=3)
     for j in (0, P - 1):
         o_ref, lse_ref = oracle.attention(q, k[:, :, j * C:(j + 1) * C].contiguous(),
-                                          v[:, :, j * C:(j + 1) * C].contiguous(), True, kv_off=j * C, rows=rows)
+                                          v[:, :, j * C:(j + 1) * C].contiguous(), causal, kv_off=j * C, rows=rows)
         check_lse(gather_rows(l1[j], rows), lse_ref)
         fin = ~np.isneginf(lse_ref)
         check_o(gather_rows(o1[j], rows).numpy()[fin], o_ref[fin], bf16_out=False)
